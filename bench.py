@@ -1,0 +1,489 @@
+"""Benchmark: dense tensor-core GEMM C = A * B^T on GB300, through the library's C ABI.
+
+Default workload: BF16 M = N = K = 8192 (the headline configuration), entries uniform in
+[-1, 1] from seed 2, FP32 accumulation, BF16 output. One step = one GEMM call on the
+next of R rotating input sets whose total footprint exceeds 2x L2, so no step reads
+operands left in L2 by the previous one.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1..c5] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). --impl reference times the CPU oracle (FP64, OpenMP over the
+host cores) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+CONFIGS = {
+    "c1": dict(kind="bf16", M=256, N=256, K=256, seed=0, workload="bf16_gemm_256x256x256"),
+    "c2": dict(kind="bf16", M=4096, N=4096, K=4096, seed=1, workload="bf16_gemm_4096x4096x4096"),
+    "c3": dict(kind="bf16", M=8192, N=8192, K=8192, seed=2, workload="bf16_gemm_8192x8192x8192"),
+    "c4": dict(kind="bf16", M=4000, N=14336, K=4096, seed=3, workload="bf16_gemm_4000x14336x4096_ragged"),
+    "c5": dict(kind="nvfp4", M=8192, N=8192, K=8192, seed=4, workload="nvfp4_gemm_8192x8192x8192"),
+}
+# The page's own number for this metric and workload: "Achieve cuBLAS Performance on NVIDIA
+# GB300 for HGEMM", Performance table, v7 at M = N = K = 8192 on GB300.
+PAGE_BASELINE = {"c3": 1980.925}
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor rates (6x)
+KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu", "csrc/gemm_nvfp4.cu"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "dense_tensor_core_persistent_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == cur:
+                return int(parts[2])
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if uuid:
+            cmd += ["-i", uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def wait_first_sample(self, timeout=5.0):
+        t = time.time()
+        while self.proc and not self.rows and time.time() - t < timeout:
+            time.sleep(0.05)
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [r for (t, r) in self.rows if self.t0 is not None and self.t0 <= t <= (self.t1 or t)]
+        rows = inside or [r for (_, r) in self.rows]
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_median": statistics.median(power) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if n_gpus > 0 else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ workloads
+
+def make_inputs(cfg, r, device):
+    import synthetic_inputs as si
+    seed = si.rotation_seed(cfg["seed"], r)
+    if cfg["kind"] == "bf16":
+        return si.bf16_problem(seed, cfg["M"], cfg["N"], cfg["K"], device=device)
+    return si.nvfp4_problem(seed, cfg["M"], cfg["N"], cfg["K"], device=device)
+
+
+def set_bytes(cfg):
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    if cfg["kind"] == "bf16":
+        return 2 * (M * K + N * K) + 2 * M * N
+    return (M * K + N * K) // 2 + (M * K + N * K) // 16 + 2 * M * N
+
+
+def launch(g, cfg, ins, C, stream, opts):
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    if cfg["kind"] == "bf16":
+        g.gemm_bf16(ins[0], ins[1], C, M, N, K, stream, opts)
+    else:
+        g.gemm_nvfp4(ins[0], ins[1], ins[2], ins[3], C, M, N, K, stream, opts)
+
+
+def oracle_rows(cfg, ins_cpu, rows):
+    import oracle
+    if cfg["kind"] == "bf16":
+        return oracle.gemm_bf16(ins_cpu[0], ins_cpu[1], 0, rows)
+    return oracle.gemm_nvfp4(*ins_cpu, 0, rows)
+
+
+def cpu_baseline(cfg, target_s=10.0):
+    """The oracle as it stands on the host cores, on a bounded sample: the first `rows` rows
+    of C (all N columns, full K). Rows are sized from a short calibration run."""
+    import oracle
+    import synthetic_inputs as si
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    oracle.build()
+    cal = min(M, 4 * oracle.num_threads())
+    ins_cpu = make_sample_inputs(cfg, cal)
+    t = time.perf_counter()
+    oracle_rows(cfg, ins_cpu, cal)
+    t_cal = max(time.perf_counter() - t, 1e-4)
+    rows = int(max(1, min(M, cal * target_s / t_cal)))
+    ins_cpu = make_sample_inputs(cfg, rows)
+    t = time.perf_counter()
+    oracle_rows(cfg, ins_cpu, rows)
+    dt = time.perf_counter() - t
+    flops = 2.0 * rows * N * K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"first {rows} of {M} rows of C (all {N} columns, K={K}), FP64, {dt:.1f} s",
+            "seconds": dt, "rows": rows}
+
+
+def make_sample_inputs(cfg, rows):
+    """Rows 0..rows-1 of A (and SFA) plus all of B (and SFB) of rotation set 0, on the host."""
+    import synthetic_inputs as si
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    seed = cfg["seed"]
+    if cfg["kind"] == "bf16":
+        A = si.uniform_bf16(seed, si.TENSOR_A, rows, K)
+        B = si.uniform_bf16(seed, si.TENSOR_B, N, K)
+        return (A, B)
+    a = si.e2m1_codes_packed(seed, si.TENSOR_A, rows, K)
+    b = si.e2m1_codes_packed(seed, si.TENSOR_B, N, K)
+    sfa = si.e4m3_scales(seed, si.TENSOR_SFA, rows, K // 16)
+    sfb = si.e4m3_scales(seed, si.TENSOR_SFB, N, K // 16)
+    return (a, sfa, b, sfb)
+
+
+# ------------------------------------------------------------------ arms
+
+def oracle_at(cfg, ins_cpu, rows, cols):
+    import oracle
+    if cfg["kind"] == "bf16":
+        return oracle.gemm_bf16_at(ins_cpu[0], ins_cpu[1], rows, cols)
+    return oracle.gemm_nvfp4_at(*ins_cpu, rows, cols)
+
+
+def run_reference(args, cfg, world, rank):
+    """The oracle as it stands, on the host cores: each step computes a fixed bounded sample
+    of output elements of the workload (sized so warm-up + timed steps take about 2 minutes)."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    oracle.build()
+    sample_rows = min(M, 64)
+    ins_cpu = make_sample_inputs(cfg, sample_rows)
+    rng = np.random.default_rng(cfg["seed"])
+    total = args.steps + args.warmup
+    budget = 120.0
+    cal = 256
+    rows, cols = rng.integers(0, sample_rows, cal), rng.integers(0, N, cal)
+    oracle_at(cfg, ins_cpu, rows, cols)
+    t = time.perf_counter()
+    oracle_at(cfg, ins_cpu, rows, cols)
+    per_elem = max((time.perf_counter() - t) / cal, 1e-8)
+    n = int(max(16, min(M * N, budget / total / per_elem)))
+    rows, cols = rng.integers(0, sample_rows, n), rng.integers(0, N, n)
+    for _ in range(args.warmup):
+        oracle_at(cfg, ins_cpu, rows, cols)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_at(cfg, ins_cpu, rows, cols)
+    dt = time.perf_counter() - t
+    value = 2.0 * n * K * args.steps / dt / 1e12
+    sample = f"each step: {n} output elements of C (K={K} each) at fixed random coordinates, FP64"
+    line = {
+        "impl": "reference",
+        "metric": metric_name(cfg), "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg["workload"], "M": M, "N": N, "K": K, "sample_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def metric_name(cfg):
+    if cfg["kind"] == "bf16":
+        return f"BF16 GEMM TFLOP/s @ M={cfg['M']} N={cfg['N']} K={cfg['K']} on 1 GB300"
+    return f"NVFP4 GEMM TFLOP/s @ M={cfg['M']} N={cfg['N']} K={cfg['K']} on 1 GB300"
+
+
+def run_ours(args, cfg, world, rank, local):
+    import torch
+
+    import dense_tensor_core_persistent_gb300 as g
+    from dense_tensor_core_persistent_gb300 import build as gbuild
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    sb = set_bytes(cfg)
+    R = max(3, math.ceil(2 * l2 / sb) + 1)
+    sets = [make_inputs(cfg, r, dev) for r in range(R)]
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    stream = torch.cuda.Stream(device=dev)
+    opts = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
+                     persistent=0 if args.no_persistent else 1)
+    flops = 2.0 * M * N * K
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            launch(g, cfg, sets[i % R], outs[i % R], stream, opts)
+    stream.synchronize()
+    st, detail = g.get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"kernel status {st} ({detail:#x}) during warm-up")
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid if rank == 0 else None) if rank == 0 else None
+    if clocks:
+        clocks.wait_first_sample()
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = g.launch_count()
+    if clocks:
+        clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        launch(g, cfg, sets[i % R], outs[i % R], stream, opts)
+    ev1.record(stream)
+    stream.synchronize()
+    if clocks:
+        clocks.mark_end()
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = g.launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    st, detail = g.get_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"kernel status {st} ({detail:#x}) in the timed region")
+    clock_info = clocks.summary() if clocks else None
+
+    per_launch_s = ms / 1e3 / args.steps
+    value = flops * args.steps * world / (ms / 1e3) / 1e12
+
+    # ---- end to end through the C ABI with host buffers: H2D inputs, GEMM, D2H result
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    host_in = [t.cpu().pin_memory() for t in sets[0]]
+    host_out = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    dev_in = [torch.empty_like(t) for t in sets[0]]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        launch(g, cfg, dev_in, outs[0], stream, opts)
+        host_out.copy_(outs[0], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = flops * e2e_steps * world / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        return
+
+    peaks, peak_src = load_peaks()
+    if cfg["kind"] == "bf16":
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_note = f"{peak_src} cuBLAS BF16 8192^3 burst (MEASURED_PEAKS bf16_tflops)"
+    else:
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * NOMINAL_FP4_OVER_BF16
+        peak_note = f"{peak_src} BF16 burst x nominal FP4/BF16 ratio 6"
+    achieved = flops / per_launch_s / 1e12
+    traffic = recorded_traffic(cfg["workload"])
+    cpu = cpu_baseline(cfg, args.cpu_seconds) if not args.no_cpu_baseline else None
+    if cpu:
+        cpu.pop("seconds", None)
+        cpu.pop("rows", None)
+    baseline = PAGE_BASELINE.get(args.config)
+    line = {
+        "metric": metric_name(cfg),
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": (value / world / baseline) if baseline else None,
+        "dtype": "bf16" if cfg["kind"] == "bf16" else "nvfp4",
+        "data": "synthetic: seeded SplitMix64 operands with the workload's value distribution",
+        "config": {
+            "workload": cfg["workload"], "M": M, "N": N, "K": K,
+            "l2_flush": f"rotation over {R} input sets of {sb / 2**20:.0f} MiB (> 2x L2 = {2 * l2 / 2**20:.0f} MiB)",
+            "kernel": {0: "default (2-CTA persistent)", 1: "1-CTA", 2: "2-CTA"}[args.kernel]
+            + ("" if not args.no_persistent else ", one tile per cluster"),
+            "baseline": "HGEMM v7 on GB300, 1980.925 TFLOP/s (page 1 Performance table)" if baseline else None,
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": achieved,
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "peak_source": peak_note,
+            "algorithmic_flops_per_launch": flops,
+        },
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": int(launches),
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=300)
+    ap.add_argument("--config", default="c3", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", type=int, default=0)
+    ap.add_argument("--group-m", type=int, default=0)
+    ap.add_argument("--max-clusters", type=int, default=0)
+    ap.add_argument("--no-persistent", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    cfg = CONFIGS[args.config]
+    world, rank, local = dist_setup(args.gpus if args.impl == "ours" else 0)
+    if args.impl == "reference":
+        run_reference(args, cfg, world, rank)
+    else:
+        run_ours(args, cfg, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,195 @@
+"""Python binding of the GB300 (sm_103a) dense tensor-core GEMM library.
+
+Argument marshalling only: every step of the GEMM runs in the CUDA kernels of
+``_lib/libdtcp_gemm.so`` (built by ``build.py``), called through its C ABI
+(``include/gemm.h``). There is no CPU or PyTorch fallback: if the library is
+missing, importing the binding's functions raises.
+
+Functions take raw device pointers (ints) or torch CUDA tensors; ``stream``
+defaults to torch's current CUDA stream when torch is importable, else the
+legacy default stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libdtcp_gemm.so")
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED_SHAPE = 2
+GEMM_ERR_MISALIGNED = 3
+GEMM_ERR_NO_DEVICE = 4
+GEMM_ERR_ARCH = 5
+GEMM_ERR_DRIVER = 6
+GEMM_ERR_LAUNCH = 7
+GEMM_ERR_TIMEOUT = 8
+
+GEMM_KERNEL_DEFAULT = 0
+GEMM_KERNEL_BF16_1CTA = 1
+GEMM_KERNEL_BF16_2CTA = 2
+
+# Entry points declared in include/gemm.h (the CPU tests check the library exports all of them).
+EXPORTS = (
+    "gemm_bf16", "gemm_nvfp4", "gemm_status_string", "gemm_get_device_status", "gemm_bf16_ex",
+    "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
+)
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class gemm_options_t(ctypes.Structure):
+    _fields_ = [
+        ("kernel", ctypes.c_int),
+        ("persistent", ctypes.c_int),
+        ("group_m", ctypes.c_int),
+        ("max_clusters", ctypes.c_int),
+        ("wait_limit_us", ctypes.c_uint32),
+        ("debug_flags", ctypes.c_uint32),
+        ("reserved", ctypes.c_int * 4),
+    ]
+
+
+def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0):
+    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags)
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with `python -m dense_tensor_core_persistent_gb300.build` "
+                "(the GEMM has no CPU fallback)")
+        l = ctypes.CDLL(LIB_PATH)
+        P, I = ctypes.c_void_p, ctypes.c_int
+        l.gemm_bf16.argtypes = [P, P, P, I, I, I, P]
+        l.gemm_bf16.restype = I
+        l.gemm_bf16_ex.argtypes = [P, P, P, I, I, I, P, ctypes.POINTER(gemm_options_t)]
+        l.gemm_bf16_ex.restype = I
+        l.gemm_nvfp4.argtypes = [P, P, P, P, P, I, I, I, P]
+        l.gemm_nvfp4.restype = I
+        l.gemm_nvfp4_ex.argtypes = [P, P, P, P, P, I, I, I, P, ctypes.POINTER(gemm_options_t)]
+        l.gemm_nvfp4_ex.restype = I
+        l.gemm_status_string.argtypes = [I]
+        l.gemm_status_string.restype = ctypes.c_char_p
+        l.gemm_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        l.gemm_get_device_status.restype = I
+        l.gemm_tile_coord.argtypes = [I, I, I, I, I, I, ctypes.POINTER(I), ctypes.POINTER(I)]
+        l.gemm_tile_coord.restype = I
+        l.gemm_choose_group_m.argtypes = [I, I, I, I, I, I, I, ctypes.c_longlong]
+        l.gemm_choose_group_m.restype = I
+        l.gemm_launch_count.argtypes = []
+        l.gemm_launch_count.restype = ctypes.c_ulonglong
+        _lib = l
+    return _lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            return 0
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != GEMM_OK:
+        raise GemmError(status, where)
+
+
+def status_string(status: int) -> str:
+    return lib().gemm_status_string(status).decode()
+
+
+def gemm_bf16(A, B, C, M: int, N: int, K: int, stream=None, opts: gemm_options_t | None = None) -> None:
+    """C[M,N] = A[M,K] @ B[N,K]^T in BF16 (FP32 accumulation); see include/gemm.h."""
+    l = lib()
+    if opts is None:
+        st = l.gemm_bf16(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream))
+    else:
+        st = l.gemm_bf16_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream), ctypes.byref(opts))
+    _check(st, "gemm_bf16")
+
+
+def gemm_nvfp4(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None, opts: gemm_options_t | None = None) -> None:
+    """C[M,N] = dequant(A, SFA) @ dequant(B, SFB)^T for packed E2M1 with per-16 E4M3 scales."""
+    l = lib()
+    if opts is None:
+        st = l.gemm_nvfp4(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _stream(stream))
+    else:
+        st = l.gemm_nvfp4_ex(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _stream(stream),
+                             ctypes.byref(opts))
+    _check(st, "gemm_nvfp4")
+
+
+def get_device_status(stream=None) -> tuple[int, int]:
+    """(status, detail word) reported by kernels since the last call; synchronises the stream."""
+    detail = ctypes.c_uint32(0)
+    st = lib().gemm_get_device_status(_stream(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def tile_coord(M, N, tile_m, tile_n, group_m, t) -> tuple[int, int]:
+    mb, nb = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().gemm_tile_coord(M, N, tile_m, tile_n, group_m, t, ctypes.byref(mb), ctypes.byref(nb)),
+           "gemm_tile_coord")
+    return mb.value, nb.value
+
+
+def choose_group_m(M, N, K, tile_m, tile_n, elem_bytes_x2, concurrent_tiles, l2_bytes) -> int:
+    g = lib().gemm_choose_group_m(M, N, K, tile_m, tile_n, elem_bytes_x2, concurrent_tiles, l2_bytes)
+    if g < 0:
+        raise GemmError(-g, "gemm_choose_group_m")
+    return g
+
+
+def launch_count() -> int:
+    return lib().gemm_launch_count()
+
+
+# ---------------------------------------------------------------- torch-tensor conveniences
+
+def matmul_bf16(A, B, out=None, stream=None, opts=None):
+    """A (M x K) and B (N x K) BF16 CUDA tensors -> C = A @ B^T (M x N BF16)."""
+    import torch
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    gemm_bf16(A, B, out, M, N, K, stream, opts)
+    return out
+
+
+def matmul_nvfp4(A, SFA, B, SFB, out=None, stream=None, opts=None):
+    """Packed E2M1 A (M x K/2), B (N x K/2) with E4M3 scales (M x K/16, N x K/16) -> BF16 C."""
+    import torch
+    M = A.shape[0]
+    N = B.shape[0]
+    K = 2 * A.shape[1]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    gemm_nvfp4(A, SFA, B, SFB, out, M, N, K, stream, opts)
+    return out

@@ -1,0 +1,293 @@
+// api.cu -- the extern "C" entry points declared in include/gemm.h: argument validation,
+// device facts, tensor-map encoding (cuTensorMapEncodeTiled through the runtime's driver
+// entry point, so the library needs no -lcuda), the device status word, and the host
+// helpers for the tile order.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/gemm.h"
+#include "host_common.h"
+#include "schedule.h"
+
+namespace dtcp {
+
+// ---------------------------------------------------------------- status word
+
+// One word per device (a static __device__ variable: nothing is allocated). Kernels
+// store the first error they hit; gemm_get_device_status reads and clears it.
+__device__ unsigned g_status_word;
+
+unsigned* device_status_word(int device) {
+  static std::mutex mu;
+  static unsigned* addr[64] = {nullptr};
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[device] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[device] = static_cast<unsigned*>(p);
+  }
+  return addr[device];
+}
+
+// ---------------------------------------------------------------- device facts
+
+const DeviceInfo* current_device_info(int* device, int* err) {
+  static std::mutex mu;
+  static DeviceInfo infos[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    *err = GEMM_ERR_NO_DEVICE;
+    return nullptr;
+  }
+  *device = dev;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    DeviceInfo d;
+    int l2 = 0;
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      *err = GEMM_ERR_NO_DEVICE;
+      return nullptr;
+    }
+    d.l2_bytes = l2;
+    infos[dev] = d;
+    have[dev] = true;
+  }
+  const DeviceInfo* d = &infos[dev];
+  // The kernels are built for sm_103a only (tcgen05, CTA pairs, 227 KB of shared memory).
+  if (d->cc_major != 10 || d->cc_minor != 3) {
+    *err = GEMM_ERR_ARCH;
+    return nullptr;
+  }
+  return d;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+std::atomic<unsigned long long> g_launches{0};
+
+}  // namespace
+
+int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
+                   uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                   CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_DRIVER;
+  const cuuint64_t dims[2] = {inner_elems, outer_rows};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  // Out-of-bounds elements of a load are filled with zeros ("NONE" = no NaN request),
+  // which leaves every sum unchanged; out-of-bounds elements of a store are dropped.
+  const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- tile order
+
+int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,
+                   double extra_bytes_per_row_k, int concurrent_tiles, long long l2_bytes) {
+  const int num_m = ceil_div(M, tile_m);
+  const int num_n = ceil_div(N, tile_n);
+  if (num_m <= 1 || num_n <= 1) return std::max(num_m, 1);
+  const double per_k = bytes_per_row_elem + extra_bytes_per_row_k;
+  const double a_total = double(M) * K * per_k, b_total = double(N) * K * per_k;
+  // Both operands fit in L2: any order re-reads from L2 only; walk all of M per column.
+  if (a_total + b_total <= double(l2_bytes)) return num_m;
+  // Bytes of one A tile and one B tile over the whole K.
+  const double w_a = double(tile_m) * K * per_k, w_b = double(tile_n) * K * per_k;
+  const int c = std::max(concurrent_tiles, 1);
+  // A wave of c consecutive tiles touches g A tiles and about c/g B tiles; equal bytes
+  // of A and B (the smallest footprint) at g = sqrt(c * w_b / w_a).
+  int g = static_cast<int>(std::lround(std::sqrt(double(c) * w_b / w_a)));
+  g = std::min(std::max(g, 1), num_m);
+  auto footprint = [&](int gg) { return gg * w_a + std::ceil(double(c) / gg) * w_b; };
+  // Shrink toward balance-preserving smaller groups while the wave does not fit in L2.
+  while (g > 1 && footprint(g) > double(l2_bytes)) --g;
+  return g;
+}
+
+// ---------------------------------------------------------------- validation helpers
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int resolve_options(const gemm_options_t* o, RunOptions* r) {
+  if (o == nullptr) return GEMM_OK;
+  for (int i = 0; i < 4; ++i)
+    if (o->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
+  if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA) return GEMM_ERR_INVALID_ARG;
+  if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
+    return GEMM_ERR_INVALID_ARG;
+  if (o->debug_flags & ~1u) return GEMM_ERR_INVALID_ARG;
+  r->kernel = o->kernel;
+  r->persistent = o->persistent;
+  r->group_m = o->group_m;
+  r->max_clusters = o->max_clusters;
+  if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
+  r->debug_flags = o->debug_flags;
+  return GEMM_OK;
+}
+
+// C = 0 for an empty K (the sum over no terms); BF16 zero is the all-zero bit pattern.
+static int zero_output(void* C, int M, int N, cudaStream_t stream) {
+  if (cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 2, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace dtcp
+
+using namespace dtcp;
+
+extern "C" {
+
+int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
+                 const gemm_options_t* options) {
+  RunOptions opt;
+  int st = resolve_options(options, &opt);
+  if (st != GEMM_OK) return st;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return GEMM_ERR_INVALID_ARG;
+  if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_MISALIGNED;
+  int device = 0, err = 0;
+  if (current_device_info(&device, &err) == nullptr) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(C, M, N, s);
+  return run_gemm_bf16(A, B, C, M, N, K, s, opt);
+}
+
+int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* stream) {
+  return gemm_bf16_ex(A, B, C, M, N, K, stream, nullptr);
+}
+
+int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                  void* stream, const gemm_options_t* options) {
+  RunOptions opt;
+  int st = resolve_options(options, &opt);
+  if (st != GEMM_OK) return st;
+  if (opt.kernel != GEMM_KERNEL_DEFAULT) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr || SFA == nullptr || SFB == nullptr)))
+    return GEMM_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))))
+    return GEMM_ERR_MISALIGNED;
+  int device = 0, err = 0;
+  if (current_device_info(&device, &err) == nullptr) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(C, M, N, s);
+  return run_gemm_nvfp4(A, SFA, B, SFB, C, M, N, K, s, opt);
+}
+
+int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+               void* stream) {
+  return gemm_nvfp4_ex(A, SFA, B, SFB, C, M, N, K, stream, nullptr);
+}
+
+const char* gemm_status_string(int status) {
+  switch (status) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case GEMM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case GEMM_ERR_NO_DEVICE: return "no CUDA device";
+    case GEMM_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case GEMM_ERR_DRIVER: return "tensor map encoding failed";
+    case GEMM_ERR_LAUNCH: return "kernel launch failed";
+    case GEMM_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int gemm_get_device_status(void* stream, uint32_t* detail) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  unsigned word = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof(word)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  if (detail) *detail = word;
+  return static_cast<int>(word & 0xFFu);
+}
+
+int gemm_tile_coord(int M, int N, int tile_m, int tile_n, int group_m, int t, int* m_blk, int* n_blk) {
+  if (M <= 0 || N <= 0 || tile_m <= 0 || tile_n <= 0 || group_m <= 0 || m_blk == nullptr || n_blk == nullptr)
+    return GEMM_ERR_INVALID_ARG;
+  const int num_m = ceil_div(M, tile_m), num_n = ceil_div(N, tile_n);
+  if (t < 0 || static_cast<long long>(t) >= static_cast<long long>(num_m) * num_n) return GEMM_ERR_INVALID_ARG;
+  const TileCoord c = tile_coord(t, num_m, num_n, group_m);
+  *m_blk = c.m_blk;
+  *n_blk = c.n_blk;
+  return GEMM_OK;
+}
+
+int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_bytes_x2, int concurrent_tiles,
+                        long long l2_bytes) {
+  if (M <= 0 || N <= 0 || K <= 0 || tile_m <= 0 || tile_n <= 0 || elem_bytes_x2 <= 0 || l2_bytes <= 0)
+    return -GEMM_ERR_INVALID_ARG;
+  // elem_bytes_x2 == 1 means packed E2M1 (half a byte) plus one scale byte per 16 elements.
+  const double per = elem_bytes_x2 * 0.5;
+  const double extra = (elem_bytes_x2 == 1) ? 1.0 / 16.0 : 0.0;
+  return choose_group_m(M, N, K, tile_m, tile_n, per, extra, concurrent_tiles, l2_bytes);
+}
+
+unsigned long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

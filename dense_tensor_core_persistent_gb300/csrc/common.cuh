@@ -1,0 +1,106 @@
+// common.cuh -- pieces shared by the BF16 and NVFP4 kernels: tcgen05 descriptors,
+// bounded mbarrier waits with error reporting, and the status-word layout.
+#pragma once
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace dtcp {
+
+// Error word written by kernels: bits 0-7 status code, 8-15 role, 16-31 stage/slot.
+constexpr uint32_t kStatusTimeout = 8;  // == GEMM_ERR_TIMEOUT
+enum Role : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleScales = 4 };
+
+__host__ __device__ constexpr uint32_t status_code(uint32_t role, uint32_t index) {
+  return kStatusTimeout | (role << 8) | (index << 16);
+}
+
+// ---------------------------------------------------------------- descriptors
+
+// Shared-memory matrix descriptor (tcgen05 / sm_100 family) for a K-major operand tile
+// written by TMA with 128-byte swizzle: every row is 128 bytes of K, eight rows form a
+// 1024-byte swizzle atom, atoms are stacked along M (or N) 1024 bytes apart. The tile
+// must start on a 1024-byte boundary; a K offset inside the 128-byte row is applied by
+// adding it to the start address (the swizzle is a function of the address bits).
+// ("Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM", v1: the MMA descriptor
+// selects the 128-byte swizzle mode, 2 << 61, so the TMA-written layout and the
+// MMA-read layout coincide.)
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu)  // bits 0-13: start address / 16
+         | (static_cast<uint64_t>(1) << 16)                 // bits 16-29: leading offset (unused here)
+         | (static_cast<uint64_t>(1024 >> 4) << 32)         // bits 32-45: stride between 8-row atoms / 16
+         | (static_cast<uint64_t>(1) << 46)                 // bits 46-47: descriptor version 1
+         | (static_cast<uint64_t>(2) << 61);                // bits 61-63: 128-byte swizzle
+}
+
+// Descriptor of an unswizzled source made of 8-row x 16-byte core matrices with the
+// rows of a core matrix contiguous (16 bytes apart) and successive core matrices along
+// the row dimension `sbo_bytes` apart.
+__device__ __forceinline__ uint64_t umma_desc_plain(uint32_t smem_addr, uint32_t sbo_bytes) {
+  return static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(0) << 16) |
+         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor, kind::f16: BF16 x BF16 -> FP32, both operands K-major.
+// bits 4-5 D format (1 = F32), 7-9 A format (1 = BF16), 10-12 B format (1 = BF16),
+// 15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf4nvf4 block-scaled: E2M1 x E2M1 -> FP32 with UE4M3
+// scale factors (bit 23 = 0), both operands K-major; scale-factor ids 0 (bits 4-5, 29-30).
+// bits 7-9 / 10-12 A / B format (1 = E2M1), 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// ---------------------------------------------------------------- bounded waits
+
+struct WaitCtx {
+  volatile uint32_t* abort_flag;  // this CTA's shared abort flag
+  unsigned* status;               // device status word
+  uint64_t limit_ns;              // bound on one wait
+};
+
+static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, WaitCtx w, uint32_t code,
+                                             bool honour_abort) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      atomicCAS(w.status, 0u, code);
+      *w.abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
+// Wait until the phase with parity `parity` of `bar` has completed. Returns false if
+// the wait gave up: after `limit_ns` (the error `code` is recorded in the status word
+// and this CTA's abort flag is raised) or because another role of this CTA aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, w, code, true);
+}
+
+// Warp-collective form: every lane waits (so every lane acquires what the barrier
+// guards), and the outcome is made uniform so the warp leaves its loop together.
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+  const bool ok = wait_phase(bar, parity, w, code);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// After an abort: give copies this thread started time to land before the CTA exits.
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+}
+
+}  // namespace dtcp

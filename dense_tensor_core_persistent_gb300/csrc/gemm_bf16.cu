@@ -1,0 +1,409 @@
+// gemm_bf16.cu -- BF16 C = A * B^T on sm_103a tensor cores (tcgen05), FP32 accumulation.
+//
+// One persistent, warp-specialised kernel template:
+//   warp 0      TMA producer: fills an S-stage shared-memory ring with A and B K-slices
+//   warp 1      MMA issuer (one thread of the pair's leader CTA) + TMEM allocator
+//   warps 2..5  epilogue: TMEM -> registers -> BF16 -> swizzled smem -> TMA store
+// CG = 1: one CTA computes a 128 x 256 tile (MMA M = 128).
+// CG = 2: a CTA pair computes a 256 x 256 tile with cta_group::2 MMAs (M = 256): each
+//         CTA holds 128 rows of A and 128 rows (N-half) of B per stage, the leader's
+//         barrier counts the bytes of both CTAs, and MMA completion is multicast to both.
+// The TMEM accumulator is double buffered (2 x 256 columns): the epilogue of tile i
+// drains one slot while the MMAs of tile i+1 fill the other.
+//
+// Design sources: "Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM" (v1 swizzled
+// TMA + descriptor, v3 warp specialisation with full/empty barriers, v4 2-CTA cluster
+// MMA with multicast commit, v5 persistent kernel with a two-slot TMEM pipeline, v6
+// TMA-store epilogue with two staging buffers and grouped tile order); "Optimized B200
+// Matrix Multiplication" (section 4: the MMA issuer never waits for its own MMAs; it
+// commits to the stage's empty barrier and the producer waits only when it wraps);
+// "NVFP4 GEMM on Blackwell" (Kernel 2: leader-owned barriers, cluster-scope waits;
+// Kernel 3: continuous stage/phase counter across tiles and the TMEM-empty handoff).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace dtcp {
+
+struct Bf16Params {
+  int M, N, K;
+  int num_m_blocks, num_n_blocks, num_tiles, k_iters;
+  int group_m;
+  unsigned* status;
+  unsigned long long wait_limit_ns;
+  unsigned debug_flags;
+};
+
+template <int CG, int STAGES>
+struct Bf16Layout {
+  static constexpr int BLOCK_M = 128;              // output rows per CTA = TMEM lanes
+  static constexpr int BLOCK_N = 256;              // output columns per tile = MMA N
+  static constexpr int BLOCK_K = 64;               // BF16 elements per stage: one 128-byte swizzle row
+  static constexpr int UMMA_K = 16;                // K per tcgen05.mma kind::f16
+  static constexpr int TILE_M = BLOCK_M * CG;      // output rows per tile (per CTA pair for CG = 2)
+  static constexpr int B_ROWS = BLOCK_N / CG;      // rows of B each CTA loads per stage
+  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
+  static constexpr int B_BYTES = B_ROWS * BLOCK_K * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ACC_COLS = BLOCK_N;         // FP32 accumulator columns per TMEM slot
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;   // two slots
+  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_BUFS = 2;
+  static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;  // 32 rows x 64 BF16 columns (one swizzle row each)
+  static constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
+
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2;
+  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
+  static constexpr int SMEM_USED = OFF_ABORT + 4;
+  static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
+
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "stage tiles must keep 1024-byte alignment");
+  static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+  static_assert(TMEM_COLS <= 512, "exceeds the 512 TMEM columns of an SM");
+  static_assert(B_ROWS <= 256, "TMA box rows must not exceed 256");
+};
+
+template <int CG, int STAGES>
+__global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
+    bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                     const __grid_constant__ CUtensorMap tmap_c, const Bf16Params p) {
+  using L = Bf16Layout<CG, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // same offset in both CTAs of a pair
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const int cluster_idx = static_cast<int>(blockIdx.x) / CG;
+  const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+  const uint32_t bar_full = base + L::OFF_BAR;       // full[s]: stage s loaded (leader's copy used)
+  const uint32_t bar_empty = bar_full + 8 * STAGES;  // empty[s]: stage s consumed by the MMAs
+  const uint32_t bar_tfull = bar_empty + 8 * STAGES; // tmem_full[slot]: accumulator ready
+  const uint32_t bar_tempty = bar_tfull + 16;        // tmem_empty[slot]: accumulator drained
+  const uint32_t bar_never = bar_tempty + 16;        // nobody arrives (timeout-path test)
+  const uint32_t bar_drain = bar_never + 8;          // MMA drain after an abort
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
+  const WaitCtx wctx{abort_flag, p.status, p.wait_limit_ns};
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar_full + 8 * s, 1);
+      mbar_init(bar_empty + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_tfull + 8 * a, 1);
+      mbar_init(bar_tempty + 8 * a, L::EPI_WARPS * CG);
+    }
+    mbar_init(bar_never, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0u;
+    fence_mbarrier_init_cluster();
+    prefetch_tensormap(&tmap_a);
+    prefetch_tensormap(&tmap_b);
+    prefetch_tensormap(&tmap_c);
+  }
+  if (warp == 1) {
+    tmem_alloc<CG>(smem_u32(tmem_slot), L::TMEM_COLS);
+    tmem_relinquish<CG>();
+  }
+  tc_fence_before_sync();
+  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = cluster_idx; t < p.num_tiles && ok; t += num_clusters) {
+        const TileCoord tc = tile_coord(t, p.num_m_blocks, p.num_n_blocks, p.group_m);
+        const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
+        const int b_row = tc.n_blk * L::BLOCK_N + static_cast<int>(rank) * L::B_ROWS;
+        for (int kb = 0; kb < p.k_iters; ++kb) {
+          // First pass over the ring: parity 1 of a fresh barrier counts as complete.
+          if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, wctx, status_code(kRoleProducer, stage))) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar_full + 8 * stage;
+          const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
+          const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(full, L::STAGE_BYTES);
+            tma_load_2d(sa, &tmap_a, kb * L::BLOCK_K, a_row, full);
+            tma_load_2d(sb, &tmap_b, kb * L::BLOCK_K, b_row, full);
+          } else {
+            const uint32_t full_leader = mapa_shared(full, 0);
+            if (rank == 0) mbar_arrive_expect_tx(full, 2 * L::STAGE_BYTES);
+            tma_load_2d_pair(sa, &tmap_a, kb * L::BLOCK_K, a_row, full_leader);
+            tma_load_2d_pair(sb, &tmap_b, kb * L::BLOCK_K, b_row, full_leader);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) settle_after_abort();
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16(L::TILE_M, L::BLOCK_N);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
+      int it = 0;
+      for (int t = cluster_idx; t < p.num_tiles && ok; t += num_clusters, ++it) {
+        const uint32_t slot = static_cast<uint32_t>(it) & 1u;
+        const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+        if (!wait_phase(bar_tempty + 8 * slot, acc_phase ^ 1u, wctx, status_code(kRoleMma, 0x100 + slot))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + slot * L::ACC_COLS;
+        for (int kb = 0; kb < p.k_iters; ++kb) {
+          if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
+          const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < L::BLOCK_K / L::UMMA_K; ++kk) {
+            const uint32_t koff = kk * L::UMMA_K * 2;  // bytes inside the 128-byte swizzle row
+            mma_f16<CG>(d_tmem, umma_desc_sw128(sa + koff), umma_desc_sw128(sb + koff), IDESC,
+                        (kb | kk) != 0 ? 1u : 0u);
+          }
+          // Release the stage when these MMAs have read it; never wait here.
+          if constexpr (CG == 1) mma_commit_local(bar_empty + 8 * stage);
+          else mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if constexpr (CG == 1) mma_commit_local(bar_tfull + 8 * slot);
+        else mma_commit_pair_multicast(bar_tfull + 8 * slot, 0x3);
+      }
+      if (!ok) {
+        // let issued MMAs finish before TMEM is released
+        if constexpr (CG == 1) mma_commit_local(bar_drain);
+        else mma_commit_pair_multicast(bar_drain, 0x1);
+        wait_phase_slow(bar_drain, 0, wctx, status_code(kRoleMma, 0xFFFE), false);
+        settle_after_abort();
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3u;  // this warp may access TMEM lanes 32q .. 32q+31
+    const uint32_t epi = warp - 2u;
+    const uint32_t stage_base = base + L::OFF_EPI + epi * L::EPI_BUFS * L::EPI_BUF_BYTES;
+    const uint32_t tempty_target = (CG == 2) ? mapa_shared(bar_tempty, 0) : bar_tempty;
+    uint32_t ebuf = 0;
+    int it = 0;
+    for (int t = cluster_idx; t < p.num_tiles; t += num_clusters, ++it) {
+      const TileCoord tc = tile_coord(t, p.num_m_blocks, p.num_n_blocks, p.group_m);
+      const uint32_t slot = static_cast<uint32_t>(it) & 1u;
+      const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
+      if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
+      tc_fence_after_sync();
+      const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M + static_cast<int>(q) * 32;
+      const int col0 = tc.n_blk * L::BLOCK_N;
+      const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * L::ACC_COLS;
+      if (row0 < p.M) {
+#pragma unroll 1
+        for (int c = 0; c < L::BLOCK_N / 64; ++c) {
+          const int col = col0 + c * 64;
+          if (col >= p.N) break;
+          uint32_t lo[32], hi[32];
+          tmem_ld_32x32b_x32(taddr + c * 64, lo);
+          tmem_ld_32x32b_x32(taddr + c * 64 + 32, hi);
+          tmem_ld_wait();
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2_rn(lo[2 * i], lo[2 * i + 1]);
+            pk[16 + i] = pack_bf16x2_rn(hi[2 * i], hi[2 * i + 1]);
+          }
+          const uint32_t buf = stage_base + ebuf * L::EPI_BUF_BYTES;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
+          __syncwarp();
+          // Row `lane` of the 32 x 64 staging tile, 16-byte chunk j at position j ^ (row % 8):
+          // the 128-byte swizzle the C tensor map uses (and bank-conflict free).
+          const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
+                         pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmap_c, buf, col, row0);
+            bulk_commit_group();
+          }
+          ebuf ^= 1u;
+        }
+      }
+      // Accumulator slot drained: hand it back to the MMA issuer (leader CTA's barrier).
+      tmem_ld_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_cluster(tempty_target + 8 * slot);
+        else mbar_arrive_local(bar_tempty + 8 * slot);
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc<CG>(tmem_base, L::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------- host side
+
+namespace {
+
+template <int CG, int STAGES>
+struct Bf16Variant {
+  using L = Bf16Layout<CG, STAGES>;
+  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES>;
+
+  // Co-resident clusters per device, queried once per device.
+  static int max_active_clusters(int device) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return 0;
+    if (cache[device] > 0) return cache[device];
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(CG * 16, 1, 1);
+    cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[device] = n;
+    return n;
+  }
+
+  static int run(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
+                 const RunOptions& opt, int device, const DeviceInfo& info) {
+    CUtensorMap ta, tb, tc;
+    int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, uint64_t(K) * 2, L::BLOCK_K,
+                            L::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GEMM_OK)
+      st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::BLOCK_K, L::B_ROWS,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GEMM_OK)
+      st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GEMM_OK) return st;
+
+    Bf16Params p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = ceil_div(M, L::TILE_M);
+    p.num_n_blocks = ceil_div(N, L::BLOCK_N);
+    const long long tiles = static_cast<long long>(p.num_m_blocks) * p.num_n_blocks;
+    if (tiles > 0x7FFFFFFFLL) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    p.num_tiles = static_cast<int>(tiles);
+    p.k_iters = ceil_div(K, L::BLOCK_K);
+    p.status = device_status_word(device);
+    p.wait_limit_ns = opt.wait_limit_ns;
+    p.debug_flags = opt.debug_flags;
+    if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
+
+    const int max_clusters = max_active_clusters(device);
+    if (max_clusters <= 0) return GEMM_ERR_LAUNCH;
+    int clusters = p.num_tiles;
+    if (opt.persistent) {
+      clusters = std::min(clusters, max_clusters);
+      if (opt.max_clusters > 0) clusters = std::min(clusters, opt.max_clusters);
+    }
+    p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
+                                : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+    cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    count_launch();
+    return GEMM_OK;
+  }
+};
+
+using Bf16OneCta = Bf16Variant<1, 4>;
+using Bf16Pair = Bf16Variant<2, 6>;
+
+}  // namespace
+
+int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
+                  const RunOptions& opt) {
+  int device = 0, err = 0;
+  const DeviceInfo* info = current_device_info(&device, &err);
+  if (info == nullptr) return err;
+  switch (opt.kernel) {
+    case GEMM_KERNEL_BF16_1CTA:
+      return Bf16OneCta::run(A, B, C, M, N, K, stream, opt, device, *info);
+    case GEMM_KERNEL_DEFAULT:
+    case GEMM_KERNEL_BF16_2CTA:
+      return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
+    default:
+      return GEMM_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace dtcp

@@ -1,0 +1,54 @@
+// host_common.h -- host-side helpers shared by the launchers and the C ABI (api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/gemm.h"
+
+namespace dtcp {
+
+// Per-device facts, queried once.
+struct DeviceInfo {
+  int cc_major = 0;
+  int cc_minor = 0;
+  int num_sms = 0;
+  long long l2_bytes = 0;
+  int max_smem_optin = 0;
+};
+
+// Current device's facts; nullptr (and *err set) if the runtime call fails.
+const DeviceInfo* current_device_info(int* device, int* err);
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point (no -lcuda).
+int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
+                   uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                   CUtensorMapSwizzle swizzle);
+
+// Device address of the process-wide status word on the current device.
+unsigned* device_status_word(int device);
+
+void count_launch();
+
+// Resolved per-call options.
+struct RunOptions {
+  int kernel = GEMM_KERNEL_DEFAULT;
+  int persistent = 1;
+  int group_m = 0;
+  int max_clusters = 0;
+  uint64_t wait_limit_ns = 2000000000ull;
+  uint32_t debug_flags = 0;
+};
+
+int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
+                  const RunOptions& opt);
+int run_gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                   cudaStream_t stream, const RunOptions& opt);
+
+// Group size along M for the persistent tile order (see gemm_choose_group_m).
+int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,
+                   double extra_bytes_per_row_k, int concurrent_tiles, long long l2_bytes);
+
+}  // namespace dtcp

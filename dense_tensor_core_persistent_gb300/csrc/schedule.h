@@ -1,0 +1,42 @@
+// schedule.h -- persistent tile order, shared by the kernels (device) and the host
+// helpers/tests (gemm_tile_coord, gemm_choose_group_m).
+//
+// Output tiles are walked M-first inside groups of `group_m` consecutive M-blocks,
+// one group after another; the last group may be shorter. Consecutive tiles (those a
+// wave of co-resident clusters works on together) then share a few B tiles and a few A
+// tiles, so the operands are re-read from L2 rather than from HBM.
+// ("Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM", v6: tile-swizzle scheduling
+// walks M-tiles first within groups of SWIZZLE_GROUP; "NVFP4 GEMM on Blackwell",
+// Kernel 5: supergroup ordering for L2 reuse.)
+#pragma once
+
+#if defined(__CUDACC__)
+#define DTCP_HD __host__ __device__ __forceinline__
+#else
+#define DTCP_HD inline
+#endif
+
+namespace dtcp {
+
+struct TileCoord {
+  int m_blk;
+  int n_blk;
+};
+
+DTCP_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Tile index t (0 <= t < num_m * num_n) -> block coordinates. Requires 1 <= group_m.
+DTCP_HD TileCoord tile_coord(int t, int num_m, int num_n, int group_m) {
+  if (group_m > num_m) group_m = num_m;
+  const int per_group = group_m * num_n;       // tiles in one full group
+  const int g = t / per_group;
+  const int first_m = g * group_m;
+  const int rows = (num_m - first_m < group_m) ? (num_m - first_m) : group_m;
+  const int local = t - g * per_group;
+  TileCoord c;
+  c.m_blk = first_m + local % rows;
+  c.n_blk = local / rows;
+  return c;
+}
+
+}  // namespace dtcp

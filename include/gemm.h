@@ -1,0 +1,165 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense tensor-core GEMM library.
+ *
+ * Both GEMMs compute C = A * B^T on one GPU:
+ *   A is M x K, B is N x K, both row-major with K contiguous ("K-major");
+ *   C is M x N, row-major BF16, overwritten (no alpha/beta, no accumulate-into-C);
+ *   products are accumulated in FP32 in tensor memory and rounded to BF16
+ *   (round to nearest, ties to even) once, in the epilogue.
+ *
+ * Sources for what is computed:
+ *   gemm_bf16  -- "Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM",
+ *                 introduction: row-major C = A @ B^T, A: MxK, B: NxK, BF16
+ *                 inputs/outputs, FP32 accumulation in tensor memory.
+ *   gemm_nvfp4 -- "NVFP4 GEMM on Blackwell", section "NVFP4 Datatype": E2M1
+ *                 values with one FP8 scale factor per 16 values; section
+ *                 "Tensor Cores and Tensor Memory": the scales are applied by
+ *                 the block-scaled tensor-core MMA (scales read from TMEM).
+ *
+ * Conventions shared by every entry point:
+ *   - All matrix pointers are DEVICE pointers of the current CUDA device,
+ *     owned by the caller; the library keeps no reference after the call.
+ *   - `stream` is a cudaStream_t / CUstream handle (NULL = legacy default
+ *     stream). Calls are asynchronous: they enqueue work and return; nothing
+ *     is synchronised. Results are visible to later work on `stream`.
+ *   - The library allocates no device memory. It holds one process-wide
+ *     device status word (a static __device__ variable) that kernels set if a
+ *     bounded internal wait expires; read it with gemm_get_device_status.
+ *   - Return value: GEMM_OK (0) or a gemm_status_t code for problems found on
+ *     the host before launch. Nothing is launched when an error is returned.
+ *     Faults during execution surface through the stream like any CUDA error.
+ *   - Thread safety: calls on different streams may be made concurrently from
+ *     several host threads.
+ */
+#ifndef DTCP_GEMM_H
+#define DTCP_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,       /* null pointer with non-empty shape, negative size, bad option */
+    GEMM_ERR_UNSUPPORTED_SHAPE = 2, /* a size constraint below is violated */
+    GEMM_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+    GEMM_ERR_NO_DEVICE = 4,         /* no CUDA device / runtime error querying it */
+    GEMM_ERR_ARCH = 5,              /* current device is not compute capability 10.3 (sm_103) */
+    GEMM_ERR_DRIVER = 6,            /* cuTensorMapEncodeTiled unavailable or rejected the operand */
+    GEMM_ERR_LAUNCH = 7,            /* the kernel launch itself failed */
+    GEMM_ERR_TIMEOUT = 8            /* device side: a bounded wait inside a kernel expired */
+} gemm_status_t;
+
+/*
+ * gemm_bf16 -- C[M][N] = bf16_rne( sum_k A[m][k] * B[n][k] ), FP32 accumulation.
+ *
+ *   A: M x K BF16, row stride K elements.   B: N x K BF16, row stride K.
+ *   C: M x N BF16, row stride N elements.
+ * Constraints: M, N, K >= 0; K % 8 == 0 and N % 8 == 0 (16-byte row strides
+ * for the tensor-memory-accelerator copies); A, B, C 16-byte aligned.
+ * M and N need not be tile multiples: rows/columns past M/N are read as zeros
+ * and never written. M == 0 or N == 0: nothing to do, returns GEMM_OK.
+ * K == 0: C is set to zero (an empty sum).
+ * Kernel: persistent, warp-specialised, 2-CTA (cta_group::2) tcgen05 MMA with
+ * a 256 x 256 output tile per CTA pair, double-buffered TMEM accumulator and a
+ * TMA-store epilogue; one kernel launch per call.
+ */
+int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* stream);
+
+/*
+ * gemm_nvfp4 -- C[M][N] = bf16_rne( sum_k a(m,k) * b(n,k) ), FP32 accumulation, where
+ *   a(m,k) = e2m1(A code m,k) * e4m3(SFA[m][k/16]),  b(n,k) = e2m1(B code n,k) * e4m3(SFB[n][k/16]).
+ *
+ *   A:   M x K/2 bytes, row-major; byte j of row m holds the E2M1 code of
+ *        element 2j in bits 0-3 and of element 2j+1 in bits 4-7.
+ *   B:   N x K/2 bytes, same packing.
+ *   SFA: M x K/16 bytes, row-major, E4M3 (OCP E4M3FN) scale of elements
+ *        16q .. 16q+15 of row m at SFA[m][q]. SFB: N x K/16 bytes, same.
+ *   C:   M x N BF16, row stride N.
+ * Constraints: M, N, K >= 0; K % 256 == 0 (one 128-byte swizzle row of codes
+ * and a 16-byte row of scales per pipeline stage); N % 8 == 0; all pointers
+ * 16-byte aligned. Ragged M / N as for gemm_bf16. K == 0 sets C to zero.
+ * Scales are used as the hardware's unsigned E4M3 (UE4M3): the sign bit of a
+ * scale byte must be 0; NaN scales give unspecified results.
+ */
+int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
+               int M, int N, int K, void* stream);
+
+/* Human-readable name of a gemm_status_t value (static string, never NULL). */
+const char* gemm_status_string(int status);
+
+/*
+ * gemm_get_device_status -- synchronises `stream`, then reads and clears the
+ * device status word. Returns GEMM_OK if no kernel reported a problem since
+ * the last call, else the code a kernel stored (GEMM_ERR_TIMEOUT). If
+ * `detail` is not NULL it receives the full 32-bit word (bits 8-15: the role
+ * whose wait expired, 1 = TMA producer, 2 = MMA issuer, 3 = epilogue,
+ * 4 = scale-factor producer; bits 16-31: the stage or slot index).
+ * Returns GEMM_ERR_NO_DEVICE if the synchronisation itself fails.
+ */
+int gemm_get_device_status(void* stream, uint32_t* detail);
+
+/* ---------------------------------------------------------------------------
+ * Variants and introspection (ablation studies, tests, benchmarks).
+ * ------------------------------------------------------------------------- */
+
+typedef enum {
+    GEMM_KERNEL_DEFAULT = 0,        /* what gemm_bf16 / gemm_nvfp4 launch */
+    GEMM_KERNEL_BF16_1CTA = 1,      /* BF16, cta_group::1, 128 x 256 tile per CTA */
+    GEMM_KERNEL_BF16_2CTA = 2       /* BF16, cta_group::2, 256 x 256 tile per CTA pair */
+} gemm_kernel_t;
+
+typedef struct {
+    int kernel;          /* gemm_kernel_t; GEMM_KERNEL_DEFAULT picks the default */
+    int persistent;      /* 1: grid = min(tiles, co-resident clusters); 0: one cluster per tile */
+    int group_m;         /* tile-order group size along M (>= 1); 0 = chosen from the shape */
+    int max_clusters;    /* cap on launched clusters for the persistent grid; 0 = no cap */
+    uint32_t wait_limit_us;   /* bound on each internal wait; 0 = default (2 s) */
+    uint32_t debug_flags;     /* 0 in production; 1 = make the MMA issuer wait on a barrier
+                                 nobody arrives on (exercises the timeout path) */
+    int reserved[4];     /* must be zero */
+} gemm_options_t;
+
+/* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
+int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
+                 const gemm_options_t* options);
+
+/* gemm_nvfp4 with explicit options (only persistent, group_m, max_clusters,
+ * wait_limit_us and debug_flags apply; kernel must be GEMM_KERNEL_DEFAULT). */
+int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
+                  int M, int N, int K, void* stream, const gemm_options_t* options);
+
+/*
+ * gemm_tile_coord -- host evaluation of the persistent tile order used by the
+ * kernels (no GPU needed). The output is split into ceil(M/tile_m) x
+ * ceil(N/tile_n) tiles; tile index t (0 <= t < tiles) is mapped to the block
+ * coordinates (*m_blk, *n_blk). Tiles are walked M-first inside groups of
+ * group_m consecutive M-blocks, group after group; the last group may be
+ * shorter ("Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM", v6 tile
+ * swizzle). Returns GEMM_ERR_INVALID_ARG for out-of-range arguments.
+ */
+int gemm_tile_coord(int M, int N, int tile_m, int tile_n, int group_m, int t, int* m_blk, int* n_blk);
+
+/*
+ * gemm_choose_group_m -- the group size the library picks for a problem when
+ * options->group_m is 0. Balances the bytes of A and B that the co-resident
+ * tiles of one wave touch, and shrinks the group until that wave footprint
+ * fits in the L2 cache ("NVFP4 GEMM on Blackwell", Production Kernel,
+ * "Supergroup Size", with the roles of M and N exchanged because the groups
+ * here run along M). elem_bytes_x2 is twice the bytes per operand element
+ * (4 for BF16, 1 for packed E2M1 plus the scale bytes counted separately:
+ * pass 1 and the function adds K/16 scale bytes per row).
+ */
+int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_bytes_x2,
+                        int concurrent_tiles, long long l2_bytes);
+
+/* Number of kernel launches this library has issued in this process (all devices). */
+unsigned long long gemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTCP_GEMM_H */

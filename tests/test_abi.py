@@ -1,0 +1,112 @@
+"""The C-ABI library without a GPU: exports, argument checks, tile order (no compute)."""
+import itertools
+import os
+import re
+
+import pytest
+
+import dense_tensor_core_persistent_gb300 as g
+from dense_tensor_core_persistent_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    gbuild.build()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w ]+?\*?\s*\b(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    declared = _header_functions()
+    assert len(declared) >= 9
+    l = g.lib()
+    for name in declared:
+        assert hasattr(l, name), name
+    assert sorted(declared) == sorted(g.EXPORTS)
+
+
+def test_status_strings():
+    for code in range(9):
+        assert g.status_string(code)
+    assert g.status_string(8) == "device wait timed out"
+    assert g.status_string(99) == "unknown status"
+
+
+def test_argument_errors_are_reported_before_any_device_use():
+    l = g.lib()
+    assert l.gemm_bf16(0, 0, 0, 0, 8, 8, 0) == g.GEMM_OK            # M == 0: nothing to do
+    assert l.gemm_bf16(0, 0, 0, 8, 0, 8, 0) == g.GEMM_OK            # N == 0
+    assert l.gemm_bf16(0, 0, 0, -1, 8, 8, 0) == g.GEMM_ERR_INVALID_ARG
+    assert l.gemm_bf16(0, 0, 0, 8, 8, 8, 0) == g.GEMM_ERR_INVALID_ARG  # null pointers
+    assert l.gemm_bf16(16, 16, 16, 8, 8, 12, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # K % 8
+    assert l.gemm_bf16(16, 16, 16, 8, 12, 8, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # N % 8
+    assert l.gemm_bf16(16, 24, 8, 8, 8, 8, 0) == g.GEMM_ERR_MISALIGNED
+    assert l.gemm_nvfp4(16, 16, 16, 16, 16, 8, 8, 128, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # K % 256
+    assert l.gemm_nvfp4(16, 16, 16, 0, 16, 8, 8, 256, 0) == g.GEMM_ERR_INVALID_ARG
+    o = g.options()
+    o.reserved[0] = 1
+    with pytest.raises(g.GemmError):
+        g.gemm_bf16(16, 16, 16, 8, 8, 8, 0, o)
+    with pytest.raises(g.GemmError):
+        g.gemm_nvfp4(16, 16, 16, 16, 16, 8, 8, 256, 0, g.options(kernel=g.GEMM_KERNEL_BF16_1CTA))
+
+
+def test_valid_call_without_gpu_reports_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert g.lib().gemm_bf16(16, 16, 16, 8, 8, 8, 0) == g.GEMM_ERR_NO_DEVICE
+
+
+def _order(num_m, num_n, group):
+    return [g.tile_coord(num_m * 256, num_n * 256, 256, 256, group, t) for t in range(num_m * num_n)]
+
+
+def test_tile_order_m_first_without_groups():
+    # group = all of M: plain M-first walk ("NVFP4 GEMM on Blackwell", Kernel 5: the v4 order
+    # (m0,n0), (m1,n0), ... (m0,n1), ...)
+    assert _order(3, 2, 3) == [(0, 0), (1, 0), (2, 0), (0, 1), (1, 1), (2, 1)]
+
+
+def test_tile_order_groups_match_supergroup_sequence_transposed():
+    # The NVFP4 page's supergroup=4 walk visits (m0,n0), (m0,n1), (m0,n2), (m0,n3), (m1,n0), ...
+    # Groups here run along M, so the same sequence appears with the roles of m and n exchanged.
+    seq = _order(8, 3, 4)
+    assert seq[:9] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1), (1, 1), (2, 1), (3, 1), (0, 2)]
+    assert seq[12:14] == [(4, 0), (5, 0)]
+
+
+def test_tile_order_last_group_is_clamped():
+    seq = _order(10, 2, 4)
+    assert seq[16:] == [(8, 0), (9, 0), (8, 1), (9, 1)]
+
+
+@pytest.mark.parametrize("num_m,num_n,group", [(1, 1, 1), (7, 5, 3), (16, 56, 9), (32, 32, 16), (5, 9, 8), (3, 4, 1)])
+def test_tile_order_is_a_permutation(num_m, num_n, group):
+    seq = _order(num_m, num_n, group)
+    assert sorted(seq) == sorted(itertools.product(range(num_m), range(num_n)))
+
+
+def test_tile_order_ragged_problem_sizes():
+    # M = 4000 with 256-row tiles: 16 M-blocks, the last one holds rows 3840..3999
+    assert g.tile_coord(4000, 14336, 256, 256, 16, 15) == (15, 0)
+    with pytest.raises(g.GemmError):
+        g.tile_coord(4000, 14336, 256, 256, 16, 16 * 56)
+
+
+def test_group_choice():
+    L2 = 126 * 2 ** 20
+    # operands fit in L2: walk all of M
+    assert g.choose_group_m(4096, 4096, 4096, 256, 256, 4, 74, L2) == 16
+    # 8192^3 BF16: balanced wave sqrt(74) ~ 9 M-blocks
+    assert g.choose_group_m(8192, 8192, 8192, 256, 256, 4, 74, L2) == 9
+    # a very large K shrinks the group until a wave's operands fit
+    gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 74, L2)
+    assert 1 <= gl < 9
+    assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 74, L2) >= 1

@@ -1,0 +1,200 @@
+"""BF16 GEMM on the GPU (through the C ABI) against the CPU oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dense_tensor_core_persistent_gb300 as g
+import oracle
+import synthetic_inputs as si
+from dense_tensor_core_persistent_gb300 import build as gbuild
+from parity import assert_bf16_close, assert_bf16_exact, bits, sample_coords
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup():
+    if DEV is None:
+        pytest.skip("needs a CUDA GPU")
+    gbuild.build()
+    oracle.build()
+    torch.cuda.set_device(DEV)
+    yield
+    st, detail = g.get_device_status()
+    assert st == g.GEMM_OK, f"a kernel reported status {st} ({detail:#x})"
+
+
+VARIANTS = {
+    "pair_persistent": dict(),
+    "pair_tile_per_cluster": dict(persistent=0),
+    "single_cta": dict(kernel=g.GEMM_KERNEL_BF16_1CTA, persistent=0),
+    "single_cta_persistent": dict(kernel=g.GEMM_KERNEL_BF16_1CTA),
+}
+
+
+def run(A, B, **opt):
+    Ad, Bd = A.to(DEV), B.to(DEV)
+    C = g.matmul_bf16(Ad, Bd, opts=g.options(**opt) if opt else None)
+    torch.cuda.synchronize()
+    return bits(C)
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_c1_uniform_256(variant):
+    """256^3, entries uniform in [-1, 1] from seed 0."""
+    A, B = si.bf16_problem(0, 256, 256, 256)
+    assert_bf16_close(run(A, B, **VARIANTS[variant]), oracle.gemm_bf16(A, B), 256, variant)
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+def test_c1_integer_twin_bit_exact(variant):
+    """256^3 with integers in [-4, 4]: every FP32 partial sum is exact, so the output is too."""
+    A, B = si.bf16_problem(0, 256, 256, 256, kind="int")
+    assert_bf16_exact(run(A, B, **VARIANTS[variant]), oracle.gemm_bf16(A, B), variant)
+
+
+SHAPES = [
+    (300, 264, 200),     # ragged M, N and a partial K stage
+    (513, 520, 136),
+    (1000, 776, 1032),
+    (129, 8, 8),         # tiny N, single K stage with zero fill
+    (1, 8, 64),
+    (257, 1024, 520),
+    (2048, 264, 64),
+]
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_ragged_shapes(variant, shape):
+    M, N, K = shape
+    A, B = si.bf16_problem(M + N + K, M, N, K)
+    assert_bf16_close(run(A, B, **VARIANTS[variant]), oracle.gemm_bf16(A, B), K, f"{variant} {shape}")
+
+
+@pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 1), (3, 2), (5, 3), (7, 16)])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
+    """Few clusters, many tiles each: the stage ring and the two TMEM slots cycle across tiles."""
+    M, N, K = 1280, 1024, 456   # 5 x 4 tiles of 256 x 256, 8 K stages (last one partial)
+    A, B = si.bf16_problem(77, M, N, K)
+    C = run(A, B, kernel=kernel, max_clusters=max_clusters, group_m=group_m)
+    assert_bf16_close(C, oracle.gemm_bf16(A, B), K, f"kernel {kernel} clusters {max_clusters} group {group_m}")
+
+
+def test_integer_inputs_many_tiles_bit_exact():
+    M, N, K = 1536, 1280, 1024
+    A, B = si.bf16_problem(9, M, N, K, kind="int")
+    assert_bf16_exact(run(A, B, max_clusters=4), oracle.gemm_bf16(A, B), "int many tiles")
+
+
+def test_output_guard_band_untouched():
+    """Nothing outside the M x N output is written (ragged edges are clipped by the TMA store)."""
+    M, N, K = 300, 264, 128
+    A, B = si.bf16_problem(5, M, N, K)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), 12345.0, dtype=torch.bfloat16, device=DEV)
+    sentinel = bits(buf[:pad]).copy()
+    C = buf[pad:pad + M * N].view(M, N)
+    g.gemm_bf16(A.to(DEV), B.to(DEV), C, M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(buf[:pad]), sentinel)
+    assert np.array_equal(bits(buf[pad + M * N:]), sentinel)
+    assert_bf16_close(bits(C), oracle.gemm_bf16(A, B), K, "guard band")
+
+
+def test_empty_and_degenerate_sizes():
+    C = torch.full((16, 16), 7.0, dtype=torch.bfloat16, device=DEV)
+    A = torch.ones(16, 8, dtype=torch.bfloat16, device=DEV)
+    g.gemm_bf16(A, A, C, 0, 16, 8)        # M = 0: nothing written
+    g.gemm_bf16(A, A, C, 16, 0, 8)        # N = 0
+    torch.cuda.synchronize()
+    assert torch.all(C == 7.0)
+    g.gemm_bf16(A, A, C, 16, 16, 0)       # K = 0: empty sum
+    torch.cuda.synchronize()
+    assert torch.all(C == 0.0)
+
+
+def test_rejected_arguments():
+    A = torch.ones(64, 64, dtype=torch.bfloat16, device=DEV)
+    C = torch.empty(64, 64, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_bf16(A, A, C, 64, 64, 60)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED_SHAPE
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_bf16(A.data_ptr() + 2, A, C, 64, 64, 64)
+    assert e.value.status == g.GEMM_ERR_MISALIGNED
+
+
+def test_all_ones_full_8192_every_element_exact():
+    """Property at the full headline size: all-ones operands give C = K = 8192 everywhere."""
+    M = N = K = 8192
+    A = torch.ones(M, K, dtype=torch.bfloat16, device=DEV)
+    C = g.matmul_bf16(A, A)
+    torch.cuda.synchronize()
+    assert torch.all(C == float(K)).item()
+
+
+def _full_size_sampled(seed, M, N, K, kind="uniform", n=4096, exact=False):
+    A, B = si.bf16_problem(seed, M, N, K, kind=kind, device=DEV)
+    C = g.matmul_bf16(A, B)   # default launch: the one the benchmark times
+    torch.cuda.synchronize()
+    rows, cols = sample_coords(M, N, n, seed)
+    got = bits(C)[rows, cols]
+    ref = oracle.gemm_bf16_at(A.cpu(), B.cpu(), rows, cols)
+    if exact:
+        assert_bf16_exact(got, ref, f"{M}x{N}x{K} {kind}")
+    else:
+        assert_bf16_close(got, ref, K, f"{M}x{N}x{K}")
+
+
+def test_c2_4096_cubed_sampled():
+    _full_size_sampled(1, 4096, 4096, 4096)
+
+
+def test_c3_8192_cubed_sampled():
+    _full_size_sampled(2, 8192, 8192, 8192)
+
+
+def test_c4_ragged_4000x14336x4096_sampled():
+    _full_size_sampled(3, 4000, 14336, 4096)
+
+
+def test_c3_shape_integer_inputs_sampled_bit_exact():
+    # |partial sums| <= 16 * 8192 < 2^24: exact in FP32 at the full size
+    _full_size_sampled(2, 8192, 8192, 8192, kind="int", n=8192, exact=True)
+
+
+def test_generator_same_values_on_gpu_and_cpu():
+    a_cpu = si.uniform_bf16(3, 0, 257, 129)
+    a_gpu = si.uniform_bf16(3, 0, 257, 129, device=DEV)
+    assert torch.equal(a_cpu, a_gpu.cpu())
+    s_cpu = si.e4m3_scales(4, 2, 64, 32)
+    assert torch.equal(s_cpu, si.e4m3_scales(4, 2, 64, 32, device=DEV).cpu())
+
+
+def test_one_launch_per_call():
+    A, B = si.bf16_problem(0, 512, 512, 512, device=DEV)
+    before = g.launch_count()
+    g.matmul_bf16(A, B)
+    torch.cuda.synchronize()
+    assert g.launch_count() == before + 1
+
+
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+def test_bounded_wait_reports_timeout_and_context_survives(kernel):
+    """debug flag 1: the MMA issuer waits on a barrier nothing arrives on. The bounded wait
+    expires (100 ms), the kernel records GEMM_ERR_TIMEOUT and exits; the context stays usable."""
+    g.get_device_status()  # clear
+    A, B = si.bf16_problem(0, 512, 512, 256, device=DEV)
+    g.matmul_bf16(A, B, opts=g.options(kernel=kernel, wait_limit_us=100_000, debug_flags=1))
+    st, detail = g.get_device_status()
+    assert st == g.GEMM_ERR_TIMEOUT
+    assert (detail >> 8) & 0xFF in (1, 2, 3)   # the role whose wait ran out first
+    # the next GEMM on the same context is correct
+    A2, B2 = si.bf16_problem(1, 256, 256, 256)
+    assert_bf16_close(run(A2, B2, kernel=kernel), oracle.gemm_bf16(A2, B2), 256, "after timeout")
+    assert g.get_device_status()[0] == g.GEMM_OK

@@ -1,0 +1,133 @@
+"""NVFP4 block-scaled GEMM on the GPU (through the C ABI) against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+import dense_tensor_core_persistent_gb300 as g
+import oracle
+import synthetic_inputs as si
+from dense_tensor_core_persistent_gb300 import build as gbuild
+from parity import assert_bf16_exact, assert_nvfp4_close, bits, sample_coords
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
+E4M3_ONE = 0x38
+
+
+@pytest.fixture(scope="module", autouse=True)
+def setup():
+    if DEV is None:
+        pytest.skip("needs a CUDA GPU")
+    gbuild.build()
+    oracle.build()
+    torch.cuda.set_device(DEV)
+    yield
+    st, detail = g.get_device_status()
+    assert st == g.GEMM_OK, f"a kernel reported status {st} ({detail:#x})"
+
+
+def run(a, sfa, b, sfb, **opt):
+    C = g.matmul_nvfp4(a.to(DEV), sfa.to(DEV), b.to(DEV), sfb.to(DEV), opts=g.options(**opt) if opt else None)
+    torch.cuda.synchronize()
+    return bits(C)
+
+
+def test_code_points_through_the_tensor_cores():
+    """Row 0 of A holds the 16 E2M1 codes (unit scales); B row j is one-hot at element j:
+    C[0, j] must be code j's value, so the hardware's E2M1 decode matches the oracle's."""
+    M, N, K = 256, 256, 256
+    codes = torch.zeros(M, K, dtype=torch.uint8)
+    codes[0, :16] = torch.arange(16, dtype=torch.uint8)
+    onehot = torch.zeros(N, K, dtype=torch.uint8)
+    onehot[torch.arange(16), torch.arange(16)] = 0x2           # 1.0
+    sf = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8)
+    a, b = si.pack_e2m1(codes), si.pack_e2m1(onehot)
+    got = oracle.bf16_bits_to_f64(run(a, sf, b, sf))
+    ref = oracle.gemm_nvfp4(a, sf, b, sf)
+    assert list(got[0, :16]) == list(ref[0, :16])
+    assert np.array_equal(got, ref)
+
+
+def test_scale_placement_per_row_and_block():
+    """Distinct power-of-two scales per (row, 16-block) on all-ones codes: C[i, j] is the exact
+    dot product of the two scale rows, so a scale routed to the wrong row or block shows."""
+    M, N, K = 256, 256, 512
+    ones = torch.full((M, K), 0x2, dtype=torch.uint8)
+    a = si.pack_e2m1(ones)
+    rng = np.random.default_rng(3)
+    sfa = torch.from_numpy(rng.choice([0x30, 0x38, 0x40, 0x48], size=(M, K // 16)).astype(np.uint8))
+    sfb = torch.from_numpy(rng.choice([0x28, 0x38, 0x40], size=(N, K // 16)).astype(np.uint8))
+    assert_bf16_exact(run(a, sfa, a, sfb), oracle.gemm_nvfp4(a, sfa, a, sfb), "scale placement")
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (512, 512, 1024), (300, 264, 512), (1, 8, 256), (640, 768, 2048)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_unit_scales_bit_exact(shape):
+    """All scales 1.0: products are multiples of 1/4 and |sums| <= 36 K, exact in FP32."""
+    M, N, K = shape
+    a, _, b, _ = si.nvfp4_problem(11, M, N, K)
+    sfa = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8)
+    sfb = torch.full((N, K // 16), E4M3_ONE, dtype=torch.uint8)
+    assert_bf16_exact(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape}")
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (512, 512, 1024), (300, 264, 512), (1000, 776, 2304)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_random_scales(shape):
+    """Codes uniform over the 16 code points, scales uniform over E4M3 values in [2^-4, 2^4]."""
+    M, N, K = shape
+    a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K)
+    assert_nvfp4_close(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape}")
+
+
+@pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 2), (5, 1)])
+def test_many_tiles_per_cluster(max_clusters, group_m):
+    M, N, K = 1280, 1024, 1280    # 5 x 4 tiles, 5 K stages: the 4-stage ring wraps inside a tile
+    a, sfa, b, sfb = si.nvfp4_problem(21, M, N, K)
+    assert_nvfp4_close(run(a, sfa, b, sfb, max_clusters=max_clusters, group_m=group_m),
+                       oracle.gemm_nvfp4(a, sfa, b, sfb), f"clusters {max_clusters}")
+
+
+def test_c5_8192_cubed_sampled():
+    M = N = K = 8192
+    a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K, device=DEV)
+    C = g.matmul_nvfp4(a, sfa, b, sfb)
+    torch.cuda.synchronize()
+    rows, cols = sample_coords(M, N, 4096, 4)
+    ref = oracle.gemm_nvfp4_at(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu(), rows, cols)
+    got = bits(C)[rows, cols]
+    assert_nvfp4_close(got, ref, "C5 sampled")
+
+
+def test_c5_shape_unit_scales_sampled_bit_exact():
+    M = N = K = 8192
+    a, _, b, _ = si.nvfp4_problem(4, M, N, K, device=DEV)
+    sfa = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8, device=DEV)
+    C = g.matmul_nvfp4(a, sfa, b, sfa)
+    torch.cuda.synchronize()
+    rows, cols = sample_coords(M, N, 8192, 5)
+    ref = oracle.gemm_nvfp4_at(a.cpu(), sfa.cpu(), b.cpu(), sfa.cpu(), rows, cols)
+    assert_bf16_exact(bits(C)[rows, cols], ref, "C5 unit scales")
+
+
+def test_empty_and_rejected():
+    C = torch.full((16, 16), 3.0, dtype=torch.bfloat16, device=DEV)
+    a = torch.zeros(16, 128, dtype=torch.uint8, device=DEV)
+    sf = torch.full((16, 16), E4M3_ONE, dtype=torch.uint8, device=DEV)
+    g.gemm_nvfp4(a, sf, a, sf, C, 16, 16, 0)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0.0)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_nvfp4(a, sf, a, sf, C, 16, 16, 128)
+    assert e.value.status == g.GEMM_ERR_UNSUPPORTED_SHAPE
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    g.get_device_status()
+    a, sfa, b, sfb = si.nvfp4_problem(4, 512, 512, 512, device=DEV)
+    g.matmul_nvfp4(a, sfa, b, sfb, opts=g.options(wait_limit_us=100_000, debug_flags=1))
+    st, _ = g.get_device_status()
+    assert st == g.GEMM_ERR_TIMEOUT
+    a, sfa, b, sfb = si.nvfp4_problem(5, 256, 256, 256)
+    assert_nvfp4_close(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), "after timeout")
+    assert g.get_device_status()[0] == g.GEMM_OK
