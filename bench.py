@@ -38,12 +38,16 @@ CONFIGS = {
 PAGE_BASELINE = {"c3": 1980.925}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor rates (6x)
-KERNEL_SOURCES = ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu", "csrc/gemm_nvfp4.cu"]
+KERNEL_SOURCES = {
+    "bf16": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu"],
+    "nvfp4": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_nvfp4.cu"],
+}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kind: str) -> str:
+    """Hash of the sources the GEMM kernel of this precision is built from."""
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "dense_tensor_core_persistent_gb300", rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -58,12 +62,12 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kind: str):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    cur = kernel_source_hash()
+    cur = kernel_source_hash(kind)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -177,12 +181,19 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------------ workloads
 
-def make_inputs(cfg, r, device):
+def make_inputs(cfg, r, device, scales="blocked"):
+    """Rotation set r on the device. NVFP4 scales are drawn row-major; for the blocked path
+    they are rearranged once here by the library's pack kernel (input preparation, like
+    packing two E2M1 codes per byte), outside the timed region."""
     import synthetic_inputs as si
     seed = si.rotation_seed(cfg["seed"], r)
     if cfg["kind"] == "bf16":
         return si.bf16_problem(seed, cfg["M"], cfg["N"], cfg["K"], device=device)
-    return si.nvfp4_problem(seed, cfg["M"], cfg["N"], cfg["K"], device=device)
+    a, sfa, b, sfb = si.nvfp4_problem(seed, cfg["M"], cfg["N"], cfg["K"], device=device)
+    if scales == "blocked":
+        import dense_tensor_core_persistent_gb300 as g
+        sfa, sfb = g.pack_scales(sfa), g.pack_scales(sfb)
+    return a, sfa, b, sfb
 
 
 def set_bytes(cfg):
@@ -192,10 +203,12 @@ def set_bytes(cfg):
     return (M * K + N * K) // 2 + (M * K + N * K) // 16 + 2 * M * N
 
 
-def launch(g, cfg, ins, C, stream, opts):
+def launch(g, cfg, ins, C, stream, opts, scales="blocked"):
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     if cfg["kind"] == "bf16":
         g.gemm_bf16(ins[0], ins[1], C, M, N, K, stream, opts)
+    elif scales == "blocked":
+        g.gemm_nvfp4_blocked(ins[0], ins[1], ins[2], ins[3], C, M, N, K, stream, opts)
     else:
         g.gemm_nvfp4(ins[0], ins[1], ins[2], ins[3], C, M, N, K, stream, opts)
 
@@ -320,17 +333,17 @@ def run_ours(args, cfg, world, rank, local):
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
     sb = set_bytes(cfg)
     R = max(3, math.ceil(2 * l2 / sb) + 1)
-    sets = [make_inputs(cfg, r, dev) for r in range(R)]
+    sets = [make_inputs(cfg, r, dev, args.scales) for r in range(R)]
     outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     stream = torch.cuda.Stream(device=dev)
     opts = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
-                     persistent=0 if args.no_persistent else 1)
+                     persistent=0 if args.no_persistent else 1, no_tail_split=1 if args.no_tail_split else 0)
     flops = 2.0 * M * N * K
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            launch(g, cfg, sets[i % R], outs[i % R], stream, opts)
+            launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales)
     stream.synchronize()
     st, detail = g.get_device_status(stream)
     if st != 0:
@@ -354,7 +367,7 @@ def run_ours(args, cfg, world, rank, local):
         clocks.mark_start()
     ev0.record(stream)
     for i in range(args.steps):
-        launch(g, cfg, sets[i % R], outs[i % R], stream, opts)
+        launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales)
     ev1.record(stream)
     stream.synchronize()
     if clocks:
@@ -383,7 +396,7 @@ def run_ours(args, cfg, world, rank, local):
     def e2e_step():
         for d, h in zip(dev_in, host_in):
             d.copy_(h, non_blocking=True)
-        launch(g, cfg, dev_in, outs[0], stream, opts)
+        launch(g, cfg, dev_in, outs[0], stream, opts, args.scales)
         host_out.copy_(outs[0], non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -412,7 +425,7 @@ def run_ours(args, cfg, world, rank, local):
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * NOMINAL_FP4_OVER_BF16
         peak_note = f"{peak_src} BF16 burst x nominal FP4/BF16 ratio 6"
     achieved = flops / per_launch_s / 1e12
-    traffic = recorded_traffic(cfg["workload"])
+    traffic = recorded_traffic(cfg["workload"] + ("" if cfg["kind"] == "bf16" else f"_{args.scales}"), cfg["kind"])
     cpu = cpu_baseline(cfg, args.cpu_seconds) if not args.no_cpu_baseline else None
     if cpu:
         cpu.pop("seconds", None)
@@ -435,7 +448,12 @@ def run_ours(args, cfg, world, rank, local):
             "workload": cfg["workload"], "M": M, "N": N, "K": K,
             "l2_flush": f"rotation over {R} input sets of {sb / 2**20:.0f} MiB (> 2x L2 = {2 * l2 / 2**20:.0f} MiB)",
             "kernel": {0: "default (2-CTA persistent)", 1: "1-CTA", 2: "2-CTA"}[args.kernel]
-            + ("" if not args.no_persistent else ", one tile per cluster"),
+            + ("" if not args.no_persistent else ", one tile per cluster")
+            + (", no tail split" if args.no_tail_split else ""),
+            "scales": (None if cfg["kind"] == "bf16" else
+                       "blocked tensor-core layout (packed once at input setup)" if args.scales == "blocked"
+                       else "row-major [rows][K/16], rearranged inside the kernel"),
+            "group_m": args.group_m or "auto",
             "baseline": "HGEMM v7 on GB300, 1980.925 TFLOP/s (page 1 Performance table)" if baseline else None,
         },
         "roofline": {
@@ -468,6 +486,8 @@ def main():
     ap.add_argument("--group-m", type=int, default=0)
     ap.add_argument("--max-clusters", type=int, default=0)
     ap.add_argument("--no-persistent", action="store_true")
+    ap.add_argument("--no-tail-split", action="store_true")
+    ap.add_argument("--scales", default="blocked", choices=["blocked", "rowmajor"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -35,6 +35,7 @@ GEMM_KERNEL_BF16_2CTA = 2
 EXPORTS = (
     "gemm_bf16", "gemm_nvfp4", "gemm_status_string", "gemm_get_device_status", "gemm_bf16_ex",
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
+    "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
 )
 
 
@@ -52,12 +53,14 @@ class gemm_options_t(ctypes.Structure):
         ("max_clusters", ctypes.c_int),
         ("wait_limit_us", ctypes.c_uint32),
         ("debug_flags", ctypes.c_uint32),
-        ("reserved", ctypes.c_int * 4),
+        ("no_tail_split", ctypes.c_int),
+        ("reserved", ctypes.c_int * 3),
     ]
 
 
-def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0):
-    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags)
+def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
+            no_tail_split=0):
+    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split)
 
 
 _lib = None
@@ -89,6 +92,14 @@ def lib() -> ctypes.CDLL:
         l.gemm_tile_coord.restype = I
         l.gemm_choose_group_m.argtypes = [I, I, I, I, I, I, I, ctypes.c_longlong]
         l.gemm_choose_group_m.restype = I
+        l.gemm_nvfp4_blocked_scale_bytes.argtypes = [I, I]
+        l.gemm_nvfp4_blocked_scale_bytes.restype = ctypes.c_longlong
+        l.gemm_nvfp4_pack_scales.argtypes = [P, P, I, I, P]
+        l.gemm_nvfp4_pack_scales.restype = I
+        l.gemm_nvfp4_blocked.argtypes = [P, P, P, P, P, I, I, I, P]
+        l.gemm_nvfp4_blocked.restype = I
+        l.gemm_nvfp4_blocked_ex.argtypes = [P, P, P, P, P, I, I, I, P, ctypes.POINTER(gemm_options_t)]
+        l.gemm_nvfp4_blocked_ex.restype = I
         l.gemm_launch_count.argtypes = []
         l.gemm_launch_count.restype = ctypes.c_ulonglong
         _lib = l
@@ -145,6 +156,32 @@ def gemm_nvfp4(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None, opts: gem
     _check(st, "gemm_nvfp4")
 
 
+def nvfp4_blocked_scale_bytes(rows: int, K: int) -> int:
+    n = lib().gemm_nvfp4_blocked_scale_bytes(rows, K)
+    if n < 0:
+        raise GemmError(GEMM_ERR_UNSUPPORTED_SHAPE, "gemm_nvfp4_blocked_scale_bytes")
+    return n
+
+
+def gemm_nvfp4_pack_scales(SF, SF_blocked, rows: int, K: int, stream=None) -> None:
+    """Row-major scales [rows][K/16] -> the blocked tensor-core layout (see include/gemm.h)."""
+    _check(lib().gemm_nvfp4_pack_scales(_ptr(SF), _ptr(SF_blocked), rows, K, _stream(stream)),
+           "gemm_nvfp4_pack_scales")
+
+
+def gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M: int, N: int, K: int, stream=None,
+                       opts: gemm_options_t | None = None) -> None:
+    """gemm_nvfp4 with scales already in the blocked layout (the fast path)."""
+    l = lib()
+    if opts is None:
+        st = l.gemm_nvfp4_blocked(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
+                                  _stream(stream))
+    else:
+        st = l.gemm_nvfp4_blocked_ex(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
+                                     _stream(stream), ctypes.byref(opts))
+    _check(st, "gemm_nvfp4_blocked")
+
+
 def get_device_status(stream=None) -> tuple[int, int]:
     """(status, detail word) reported by kernels since the last call; synchronises the stream."""
     detail = ctypes.c_uint32(0)
@@ -180,6 +217,28 @@ def matmul_bf16(A, B, out=None, stream=None, opts=None):
     if out is None:
         out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
     gemm_bf16(A, B, out, M, N, K, stream, opts)
+    return out
+
+
+def pack_scales(SF, stream=None):
+    """Row-major E4M3 scales (rows x K/16 uint8 CUDA tensor) -> blocked-layout uint8 tensor."""
+    import torch
+    rows, kb = SF.shape
+    K = 16 * kb
+    out = torch.empty(nvfp4_blocked_scale_bytes(rows, K), dtype=torch.uint8, device=SF.device)
+    gemm_nvfp4_pack_scales(SF, out, rows, K, stream)
+    return out
+
+
+def matmul_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, out=None, stream=None, opts=None):
+    """Like matmul_nvfp4, with scales from pack_scales."""
+    import torch
+    M = A.shape[0]
+    N = B.shape[0]
+    K = 2 * A.shape[1]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, out, M, N, K, stream, opts)
     return out
 
 

@@ -155,8 +155,9 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o == nullptr) return GEMM_OK;
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 3; ++i)
     if (o->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
+  if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
@@ -165,6 +166,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->persistent = o->persistent;
   r->group_m = o->group_m;
   r->max_clusters = o->max_clusters;
+  r->tail_split = o->no_tail_split ? 0 : 1;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -223,12 +225,54 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   if (current_device_info(&device, &err) == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return zero_output(C, M, N, s);
-  return run_gemm_nvfp4(A, SFA, B, SFB, C, M, N, K, s, opt);
+  return run_gemm_nvfp4(A, SFA, B, SFB, C, M, N, K, s, opt, false);
 }
 
 int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
                void* stream) {
   return gemm_nvfp4_ex(A, SFA, B, SFB, C, M, N, K, stream, nullptr);
+}
+
+long long gemm_nvfp4_blocked_scale_bytes(int rows, int K) {
+  if (rows < 0 || K < 0 || K % 64 != 0) return -1;
+  return static_cast<long long>(ceil_div(rows, 128)) * 128 * (K / 16);
+}
+
+int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, void* stream) {
+  if (rows < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (K % 64 != 0 || ceil_div(rows, 128) > 65535) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (rows == 0 || K == 0) return GEMM_OK;
+  if (SF == nullptr || SF_blocked == nullptr) return GEMM_ERR_INVALID_ARG;
+  if (!aligned16(SF) || !aligned16(SF_blocked)) return GEMM_ERR_MISALIGNED;
+  int device = 0, err = 0;
+  if (current_device_info(&device, &err) == nullptr) return err;
+  return run_pack_scales(SF, SF_blocked, rows, K, static_cast<cudaStream_t>(stream));
+}
+
+int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                          int M, int N, int K, void* stream, const gemm_options_t* options) {
+  RunOptions opt;
+  int st = resolve_options(options, &opt);
+  if (st != GEMM_OK) return st;
+  if (opt.kernel != GEMM_KERNEL_DEFAULT) return GEMM_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr || SFA_blocked == nullptr || SFB_blocked == nullptr)))
+    return GEMM_ERR_INVALID_ARG;
+  if (K % 256 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(C) ||
+      (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA_blocked) || !aligned16(SFB_blocked))))
+    return GEMM_ERR_MISALIGNED;
+  int device = 0, err = 0;
+  if (current_device_info(&device, &err) == nullptr) return err;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) return zero_output(C, M, N, s);
+  return run_gemm_nvfp4(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt, true);
+}
+
+int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C, int M,
+                       int N, int K, void* stream) {
+  return gemm_nvfp4_blocked_ex(A, SFA_blocked, B, SFB_blocked, C, M, N, K, stream, nullptr);
 }
 
 const char* gemm_status_string(int status) {

@@ -33,6 +33,7 @@ namespace dtcp {
 struct Bf16Params {
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_tiles, k_iters;
+  int split_tiles, num_items;  // trailing tiles cut into N-halves; work items = tiles + split_tiles
   int group_m;
   unsigned* status;
   unsigned long long wait_limit_ns;
@@ -77,7 +78,8 @@ struct Bf16Layout {
 template <int CG, int STAGES>
 __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                     const __grid_constant__ CUtensorMap tmap_c, const Bf16Params p) {
+                     const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_c,
+                     const Bf16Params p) {
   using L = Bf16Layout<CG, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -115,6 +117,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
     fence_mbarrier_init_cluster();
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
+    prefetch_tensormap(&tmap_b_half);
     prefetch_tensormap(&tmap_c);
   }
   if (warp == 1) {
@@ -131,10 +134,15 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int t = cluster_idx; t < p.num_tiles && ok; t += num_clusters) {
-        const TileCoord tc = tile_coord(t, p.num_m_blocks, p.num_n_blocks, p.group_m);
+      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters) {
+        const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+        const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
+        const bool half = w.half >= 0;
         const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
-        const int b_row = tc.n_blk * L::BLOCK_N + static_cast<int>(rank) * L::B_ROWS;
+        const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
+                                                        : static_cast<int>(rank) * L::B_ROWS);
+        const CUtensorMap* map_b = half ? &tmap_b_half : &tmap_b;
+        const uint32_t stage_bytes = L::A_BYTES + (half ? L::B_BYTES / 2 : L::B_BYTES);
         for (int kb = 0; kb < p.k_iters; ++kb) {
           // First pass over the ring: parity 1 of a fresh barrier counts as complete.
           if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, wctx, status_code(kRoleProducer, stage))) {
@@ -145,14 +153,14 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
           const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
           if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(full, L::STAGE_BYTES);
+            mbar_arrive_expect_tx(full, stage_bytes);
             tma_load_2d(sa, &tmap_a, kb * L::BLOCK_K, a_row, full);
-            tma_load_2d(sb, &tmap_b, kb * L::BLOCK_K, b_row, full);
+            tma_load_2d(sb, map_b, kb * L::BLOCK_K, b_row, full);
           } else {
             const uint32_t full_leader = mapa_shared(full, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full, 2 * L::STAGE_BYTES);
+            if (rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
             tma_load_2d_pair(sa, &tmap_a, kb * L::BLOCK_K, a_row, full_leader);
-            tma_load_2d_pair(sb, &tmap_b, kb * L::BLOCK_K, b_row, full_leader);
+            tma_load_2d_pair(sb, map_b, kb * L::BLOCK_K, b_row, full_leader);
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -166,12 +174,14 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (rank == 0 && lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16(L::TILE_M, L::BLOCK_N);
+      constexpr uint32_t IDESC_FULL = idesc_bf16(L::TILE_M, L::BLOCK_N);
+      constexpr uint32_t IDESC_HALF = idesc_bf16(L::TILE_M, L::BLOCK_N / 2);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
       int it = 0;
-      for (int t = cluster_idx; t < p.num_tiles && ok; t += num_clusters, ++it) {
+      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
+        const uint32_t idesc = (i >= p.num_tiles - p.split_tiles) ? IDESC_HALF : IDESC_FULL;
         const uint32_t slot = static_cast<uint32_t>(it) & 1u;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
         if (!wait_phase(bar_tempty + 8 * slot, acc_phase ^ 1u, wctx, status_code(kRoleMma, 0x100 + slot))) {
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < L::BLOCK_K / L::UMMA_K; ++kk) {
             const uint32_t koff = kk * L::UMMA_K * 2;  // bytes inside the 128-byte swizzle row
-            mma_f16<CG>(d_tmem, umma_desc_sw128(sa + koff), umma_desc_sw128(sb + koff), IDESC,
+            mma_f16<CG>(d_tmem, umma_desc_sw128(sa + koff), umma_desc_sw128(sb + koff), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
           }
           // Release the stage when these MMAs have read it; never wait here.
@@ -223,18 +233,20 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
     const uint32_t tempty_target = (CG == 2) ? mapa_shared(bar_tempty, 0) : bar_tempty;
     uint32_t ebuf = 0;
     int it = 0;
-    for (int t = cluster_idx; t < p.num_tiles; t += num_clusters, ++it) {
-      const TileCoord tc = tile_coord(t, p.num_m_blocks, p.num_n_blocks, p.group_m);
+    for (int i = cluster_idx; i < p.num_items; i += num_clusters, ++it) {
+      const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+      const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
+      const int chunks = (w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N) / 64;
       const uint32_t slot = static_cast<uint32_t>(it) & 1u;
       const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
       if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
       tc_fence_after_sync();
       const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M + static_cast<int>(q) * 32;
-      const int col0 = tc.n_blk * L::BLOCK_N;
+      const int col0 = tc.n_blk * L::BLOCK_N + (w.half > 0 ? L::BLOCK_N / 2 : 0);
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * L::ACC_COLS;
       if (row0 < p.M) {
 #pragma unroll 1
-        for (int c = 0; c < L::BLOCK_N / 64; ++c) {
+        for (int c = 0; c < chunks; ++c) {
           const int col = col0 + c * 64;
           if (col >= p.N) break;
           uint32_t lo[32], hi[32];
@@ -327,12 +339,15 @@ struct Bf16Variant {
 
   static int run(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                  const RunOptions& opt, int device, const DeviceInfo& info) {
-    CUtensorMap ta, tb, tc;
+    CUtensorMap ta, tb, tbh, tc;
     int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, uint64_t(K) * 2, L::BLOCK_K,
                             L::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == GEMM_OK)
       st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::BLOCK_K, L::B_ROWS,
                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GEMM_OK)  // B box of a half-width work item
+      st = encode_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::BLOCK_K,
+                          L::B_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == GEMM_OK)
       st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -355,11 +370,16 @@ struct Bf16Variant {
 
     const int max_clusters = max_active_clusters(device);
     if (max_clusters <= 0) return GEMM_ERR_LAUNCH;
-    int clusters = p.num_tiles;
+    // Persistent grid: at most the co-resident clusters. The last partial wave is cut
+    // into N-halves when they still fit in one wave.
+    int wave = p.num_tiles;
     if (opt.persistent) {
-      clusters = std::min(clusters, max_clusters);
-      if (opt.max_clusters > 0) clusters = std::min(clusters, opt.max_clusters);
+      wave = max_clusters;
+      if (opt.max_clusters > 0) wave = std::min(wave, opt.max_clusters);
     }
+    p.split_tiles = (opt.persistent && opt.tail_split) ? tail_split_tiles(p.num_tiles, wave) : 0;
+    p.num_items = p.num_tiles + p.split_tiles;
+    const int clusters = std::min(p.num_items, wave);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
 
@@ -375,7 +395,7 @@ struct Bf16Variant {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tc, p);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return GEMM_ERR_LAUNCH;

@@ -41,7 +41,11 @@ struct Nvfp4Params {
   unsigned debug_flags;
 };
 
-template <int STAGES>
+// BLOCKED = false: scales arrive row-major ([rows][K/16]) and a scale warp rearranges them.
+// BLOCKED = true:  scales arrive already in the tcgen05.cp source layout (see
+//                  pack_scales.cu), so a stage's scales for 128 rows are one contiguous
+//                  2 KB block that the producer loads with the tiles.
+template <int STAGES, bool BLOCKED>
 struct Nvfp4Layout {
   static constexpr int CG = 2;
   static constexpr int BLOCK_M = 128;              // output rows per CTA
@@ -64,16 +68,17 @@ struct Nvfp4Layout {
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;
-  static constexpr int SF_WARP = 2 + EPI_WARPS;            // warp 6
-  static constexpr int NUM_THREADS = 32 * (3 + EPI_WARPS);
+  static constexpr int SF_WARP = 2 + EPI_WARPS;            // warp 6 (row-major scales only)
+  static constexpr int NUM_THREADS = 32 * ((BLOCKED ? 2 : 3) + EPI_WARPS);
+  static constexpr int LAND_STAGES = BLOCKED ? 0 : STAGES;
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;       // rearranged, tcgen05.cp source
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_SFA_IN = OFF_SFB + STAGES * SFB_BYTES; // TMA landing, row-major
-  static constexpr int OFF_SFB_IN = OFF_SFA_IN + STAGES * SFA_BYTES;
-  static constexpr int OFF_EPI = OFF_SFB_IN + STAGES * SFB_BYTES;
+  static constexpr int OFF_SFB_IN = OFF_SFA_IN + LAND_STAGES * SFA_BYTES;
+  static constexpr int OFF_EPI = OFF_SFB_IN + LAND_STAGES * SFB_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
   // full[S], empty[S], sf_landed[S], sf_full[S], tmem_full, tmem_empty, never, drain
   static constexpr int NUM_BARS = 4 * STAGES + 4;
@@ -103,12 +108,12 @@ __device__ __forceinline__ void rearrange_scale_block(uint32_t src_rows, uint32_
   for (int j = 0; j < 4; ++j) st_shared_v4(dst_blocks + j * 512u + lane * 16u, w[0][j], w[1][j], w[2][j], w[3][j]);
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
+template <int STAGES, bool BLOCKED>
+__global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                       const __grid_constant__ CUtensorMap tmap_c, const Nvfp4Params p) {
-  using L = Nvfp4Layout<STAGES>;
+  using L = Nvfp4Layout<STAGES, BLOCKED>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -175,10 +180,22 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
             break;
           }
           const uint32_t full = bar_full + 8 * stage;
-          if (rank == 0) mbar_arrive_expect_tx(full, 2 * (L::A_BYTES + L::B_BYTES));
+          constexpr uint32_t kStageBytes = L::A_BYTES + L::B_BYTES + (BLOCKED ? L::SFA_BYTES + L::SFB_BYTES : 0);
+          if (rank == 0) mbar_arrive_expect_tx(full, 2 * kStageBytes);
           const uint32_t full_leader = mapa_shared(full, 0);
           tma_load_2d_pair(base + L::OFF_A + stage * L::A_BYTES, &tmap_a, kb * (L::BLOCK_K / 2), a_row, full_leader);
           tma_load_2d_pair(base + L::OFF_B + stage * L::B_BYTES, &tmap_b, kb * (L::BLOCK_K / 2), b_row, full_leader);
+          if constexpr (BLOCKED) {
+            // 512-byte blocks indexed (row block, 64-K step); one stage = 4 consecutive blocks
+            const int ksteps = p.K / L::UMMA_K;
+            const int y = kb * L::KSTEPS;
+            tma_load_2d_pair(base + L::OFF_SFA + stage * L::SFA_BYTES, &tmap_sfa, 0, (a_row / 128) * ksteps + y,
+                             full_leader);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d_pair(base + L::OFF_SFB + stage * L::SFB_BYTES + h * 2048, &tmap_sfb, 0,
+                               (tc.n_blk * 2 + h) * ksteps + y, full_leader);
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -188,42 +205,38 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
       if (!ok) settle_after_abort();
     }
     __syncwarp();
-  } else if (warp == L::SF_WARP) {
+  } else if (!BLOCKED && warp == L::SF_WARP) {
     // ------------------------------------------------------------ scale-factor producer
-    // Runs up to STAGES-1 stage loads ahead of the rearrangement it does itself.
+    // Landing buffer s is refilled (TMA for stage g+STAGES) as soon as this warp has
+    // rearranged stage g out of it; only the rearranged buffer, which tcgen05.cp reads,
+    // has to wait for the MMAs of stage g-STAGES (empty barrier). The loads therefore
+    // run STAGES ahead and never wait behind MMA completion.
     const int k_iters = p.k_iters;
     const int my_tiles = (p.num_tiles - cluster_idx + num_clusters - 1) / num_clusters;
     const long long total = static_cast<long long>(my_tiles > 0 ? my_tiles : 0) * k_iters;
     const uint32_t sffull_leader = mapa_shared(bar_sffull, 0);
-    long long g_issue = 0;
-    bool ok = true;
-    for (long long g = 0; g < total && ok; ++g) {
-      // issue the scale loads of stages g .. g+STAGES-1 that are not issued yet
-      while (g_issue < total && g_issue < g + STAGES) {
-        const uint32_t s = static_cast<uint32_t>(g_issue % STAGES);
-        const uint32_t ph = static_cast<uint32_t>((g_issue / STAGES) & 1);
-        if (!wait_phase_warp(bar_empty + 8 * s, ph ^ 1u, wctx, status_code(kRoleScales, s))) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const int tile = cluster_idx + static_cast<int>(g_issue / k_iters) * num_clusters;
-          const int kb = static_cast<int>(g_issue % k_iters);
-          const TileCoord tc = tile_coord(tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
-          const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
-          const int b_row = tc.n_blk * L::BLOCK_N;
-          const uint32_t land = bar_sfland + 8 * s;
-          mbar_arrive_expect_tx(land, L::SFA_BYTES + L::SFB_BYTES);
-          tma_load_2d(base + L::OFF_SFA_IN + s * L::SFA_BYTES, &tmap_sfa, kb * L::SF_PER_ROW, a_row, land);
-          tma_load_2d(base + L::OFF_SFB_IN + s * L::SFB_BYTES, &tmap_sfb, kb * L::SF_PER_ROW, b_row, land);
-        }
-        __syncwarp();
-        ++g_issue;
+    auto issue = [&](long long gi) {
+      if (lane == 0) {
+        const uint32_t s = static_cast<uint32_t>(gi % STAGES);
+        const int tile = cluster_idx + static_cast<int>(gi / k_iters) * num_clusters;
+        const int kb = static_cast<int>(gi % k_iters);
+        const TileCoord tc = tile_coord(tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
+        const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
+        const int b_row = tc.n_blk * L::BLOCK_N;
+        const uint32_t land = bar_sfland + 8 * s;
+        mbar_arrive_expect_tx(land, L::SFA_BYTES + L::SFB_BYTES);
+        tma_load_2d(base + L::OFF_SFA_IN + s * L::SFA_BYTES, &tmap_sfa, kb * L::SF_PER_ROW, a_row, land);
+        tma_load_2d(base + L::OFF_SFB_IN + s * L::SFB_BYTES, &tmap_sfb, kb * L::SF_PER_ROW, b_row, land);
       }
-      if (!ok) break;
+      __syncwarp();
+    };
+    for (long long gi = 0; gi < total && gi < STAGES; ++gi) issue(gi);
+    bool ok = true;
+    for (long long g = 0; g < total; ++g) {
       const uint32_t s = static_cast<uint32_t>(g % STAGES);
       const uint32_t ph = static_cast<uint32_t>((g / STAGES) & 1);
-      if (!wait_phase_warp(bar_sfland + 8 * s, ph, wctx, status_code(kRoleScales, 0x100 + s))) {
+      if (!wait_phase_warp(bar_sfland + 8 * s, ph, wctx, status_code(kRoleScales, 0x100 + s)) ||
+          !wait_phase_warp(bar_empty + 8 * s, ph ^ 1u, wctx, status_code(kRoleScales, s))) {
         ok = false;
         break;
       }
@@ -235,6 +248,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
       fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp reads
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(sffull_leader + 8 * s);
+      if (g + STAGES < total) issue(g + STAGES);  // landing buffer s is free again
     }
     if (!ok) settle_after_abort();
     __syncwarp();
@@ -254,12 +268,21 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
         tc_fence_after_sync();
         for (int kb = 0; kb < p.k_iters; ++kb) {
           const uint32_t sf_col = tmem_base + L::SF_TMEM_COL0 + stage * L::SF_COLS;
-          // scales first: they are small and usually land before the tiles
-          if (!wait_phase(bar_sffull + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage))) {
-            ok = false;
-            break;
+          // scales first: they are small and usually land before the tiles (in blocked
+          // mode they travel with the tiles and the full barrier covers them)
+          if (!BLOCKED) {
+            if (!wait_phase(bar_sffull + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+          } else {
+            if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
           }
-          tc_fence_after_sync();
           const uint32_t sfa_src = base + L::OFF_SFA + stage * L::SFA_BYTES;
           const uint32_t sfb_src = base + L::OFF_SFB + stage * L::SFB_BYTES;
 #pragma unroll
@@ -270,11 +293,13 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
               tmem_cp_32x128b_warpx4<2>(sf_col + 16 + 8 * j + 4 * h,
                                         umma_desc_plain(sfb_src + h * 2048 + j * L::SF_BLOCK, 128));
           }
-          if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
-            ok = false;
-            break;
+          if (!BLOCKED) {
+            if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
           }
-          tc_fence_after_sync();
           const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
 #pragma unroll
@@ -374,111 +399,132 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
 
 namespace {
 
-constexpr int kNvfp4Stages = 4;
-using NL = Nvfp4Layout<kNvfp4Stages>;
-constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kNvfp4Stages>;
+template <int STAGES, bool BLOCKED>
+struct Nvfp4Variant {
+  using L = Nvfp4Layout<STAGES, BLOCKED>;
+  static constexpr auto kernel = nvfp4_gemm_kernel<STAGES, BLOCKED>;
 
-int nvfp4_max_active_clusters(int device) {
-  static std::mutex mu;
-  static int cache[64] = {0};
-  std::lock_guard<std::mutex> lock(mu);
-  if (device < 0 || device >= 64) return 0;
-  if (cache[device] > 0) return cache[device];
-  if (cudaFuncSetAttribute(kNvfp4Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) != cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(2 * 16, 1, 1);
-  cfg.blockDim = dim3(NL::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = NL::SMEM_BYTES;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kNvfp4Kernel, &cfg) != cudaSuccess || n <= 0) {
-    cudaGetLastError();
-    return 0;
+  static int max_active_clusters(int device) {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    if (device < 0 || device >= 64) return 0;
+    if (cache[device] > 0) return cache[device];
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(2 * 16, 1, 1);
+    cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[device] = n;
+    return n;
   }
-  cache[device] = n;
-  return n;
-}
+
+  static int run(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                 cudaStream_t stream, const RunOptions& opt, int device, const DeviceInfo& info) {
+    CUtensorMap ta, tb, tsa, tsb, tc;
+    const uint64_t kbytes = uint64_t(K) / 2, kscales = uint64_t(K) / 16;
+    int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, L::BLOCK_K / 2, L::BLOCK_M,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GEMM_OK)
+      st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, L::BLOCK_K / 2, L::B_ROWS,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (BLOCKED) {
+      // blocked scales: rows of 512-byte blocks (128 words), one block per (row block, 64-K step)
+      const uint64_t ksteps = uint64_t(K) / 64;
+      if (st == GEMM_OK)
+        st = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFA, 128, uint64_t(ceil_div(M, 128)) * ksteps,
+                            512, 128, L::KSTEPS, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st == GEMM_OK)
+        st = encode_tmap_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, 128, uint64_t(ceil_div(N, 128)) * ksteps,
+                            512, 128, L::KSTEPS, CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      if (st == GEMM_OK)
+        st = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, kscales, M, kscales, L::SF_PER_ROW, L::BLOCK_M,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (st == GEMM_OK)
+        st = encode_tmap_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, kscales, N, kscales, L::SF_PER_ROW, L::BLOCK_N,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    if (st == GEMM_OK)
+      st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GEMM_OK) return st;
+
+    Nvfp4Params p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.num_m_blocks = ceil_div(M, L::TILE_M);
+    p.num_n_blocks = ceil_div(N, L::BLOCK_N);
+    const long long tiles = static_cast<long long>(p.num_m_blocks) * p.num_n_blocks;
+    if (tiles > 0x7FFFFFFFLL) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    p.num_tiles = static_cast<int>(tiles);
+    p.k_iters = K / L::BLOCK_K;
+    p.status = device_status_word(device);
+    p.wait_limit_ns = opt.wait_limit_ns;
+    p.debug_flags = opt.debug_flags;
+    if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
+
+    const int max_clusters = max_active_clusters(device);
+    if (max_clusters <= 0) return GEMM_ERR_LAUNCH;
+    int clusters = p.num_tiles;
+    if (opt.persistent) {
+      clusters = std::min(clusters, max_clusters);
+      if (opt.max_clusters > 0) clusters = std::min(clusters, opt.max_clusters);
+    }
+    // bytes per row element: half a byte of code; plus one scale byte per 16 elements
+    p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
+                                : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 0.5, 1.0 / 16.0, clusters,
+                                                 info.l2_bytes);
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2), 1, 1);
+    cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tsa, tsb, tc, p);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_LAUNCH;
+    }
+    count_launch();
+    return GEMM_OK;
+  }
+};
+
+using Nvfp4RowMajorScales = Nvfp4Variant<4, false>;
+using Nvfp4BlockedScales = Nvfp4Variant<5, true>;
 
 }  // namespace
 
 int run_gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
-                   cudaStream_t stream, const RunOptions& opt) {
+                   cudaStream_t stream, const RunOptions& opt, bool blocked_scales) {
   int device = 0, err = 0;
   const DeviceInfo* info = current_device_info(&device, &err);
   if (info == nullptr) return err;
   if (opt.kernel != GEMM_KERNEL_DEFAULT) return GEMM_ERR_INVALID_ARG;
-
-  CUtensorMap ta, tb, tsa, tsb, tc;
-  const uint64_t kbytes = uint64_t(K) / 2, kscales = uint64_t(K) / 16;
-  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, NL::BLOCK_K / 2, NL::BLOCK_M,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, NL::BLOCK_K / 2, NL::B_ROWS,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFA, kscales, M, kscales, NL::SF_PER_ROW, NL::BLOCK_M,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT8, SFB, kscales, N, kscales, NL::SF_PER_ROW, NL::BLOCK_N,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
-  if (st != GEMM_OK) return st;
-
-  Nvfp4Params p;
-  p.M = M;
-  p.N = N;
-  p.K = K;
-  p.num_m_blocks = ceil_div(M, NL::TILE_M);
-  p.num_n_blocks = ceil_div(N, NL::BLOCK_N);
-  const long long tiles = static_cast<long long>(p.num_m_blocks) * p.num_n_blocks;
-  if (tiles > 0x7FFFFFFFLL) return GEMM_ERR_UNSUPPORTED_SHAPE;
-  p.num_tiles = static_cast<int>(tiles);
-  p.k_iters = K / NL::BLOCK_K;
-  p.status = device_status_word(device);
-  p.wait_limit_ns = opt.wait_limit_ns;
-  p.debug_flags = opt.debug_flags;
-  if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
-
-  const int max_clusters = nvfp4_max_active_clusters(device);
-  if (max_clusters <= 0) return GEMM_ERR_LAUNCH;
-  int clusters = p.num_tiles;
-  if (opt.persistent) {
-    clusters = std::min(clusters, max_clusters);
-    if (opt.max_clusters > 0) clusters = std::min(clusters, opt.max_clusters);
-  }
-  // bytes per row element: half a byte of code; plus one scale byte per 16 elements
-  p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
-                              : choose_group_m(M, N, K, NL::TILE_M, NL::BLOCK_N, 0.5, 1.0 / 16.0, clusters,
-                                               info->l2_bytes);
-
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2), 1, 1);
-  cfg.blockDim = dim3(NL::NUM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = NL::SMEM_BYTES;
-  cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kNvfp4Kernel, ta, tb, tsa, tsb, tc, p);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_LAUNCH;
-  }
-  count_launch();
-  return GEMM_OK;
+  if (blocked_scales) return Nvfp4BlockedScales::run(A, SFA, B, SFB, C, M, N, K, stream, opt, device, *info);
+  return Nvfp4RowMajorScales::run(A, SFA, B, SFB, C, M, N, K, stream, opt, device, *info);
 }
 
 }  // namespace dtcp

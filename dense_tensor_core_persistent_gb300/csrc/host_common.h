@@ -38,6 +38,7 @@ struct RunOptions {
   int persistent = 1;
   int group_m = 0;
   int max_clusters = 0;
+  int tail_split = 1;
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
 };
@@ -45,7 +46,8 @@ struct RunOptions {
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt);
 int run_gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
-                   cudaStream_t stream, const RunOptions& opt);
+                   cudaStream_t stream, const RunOptions& opt, bool blocked_scales);
+int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).
 int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,

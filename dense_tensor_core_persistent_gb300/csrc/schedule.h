@@ -39,4 +39,34 @@ DTCP_HD TileCoord tile_coord(int t, int num_m, int num_n, int group_m) {
   return c;
 }
 
+// Work items of a persistent launch: the tiles in schedule order, except that the last
+// `split_tiles` tiles are each cut into two halves along N. The halves form the final
+// partial wave, which then occupies twice as many clusters for half as long.
+struct WorkItem {
+  int tile;
+  int half;  // -1: the whole tile; 0 / 1: the lower / upper half of its columns
+};
+
+DTCP_HD WorkItem work_item(int i, int num_tiles, int split_tiles) {
+  const int whole = num_tiles - split_tiles;
+  WorkItem w;
+  if (i < whole) {
+    w.tile = i;
+    w.half = -1;
+  } else {
+    const int j = i - whole;
+    w.tile = whole + (j >> 1);
+    w.half = j & 1;
+  }
+  return w;
+}
+
+// How many trailing tiles to split for a grid of `clusters` co-resident clusters: the
+// last wave's tiles, when their halves still fit in one wave.
+DTCP_HD int tail_split_tiles(int num_tiles, int clusters) {
+  if (clusters <= 1 || num_tiles <= 0) return 0;
+  const int tail = num_tiles % clusters;
+  return (tail > 0 && 2 * tail <= clusters) ? tail : 0;
+}
+
 }  // namespace dtcp

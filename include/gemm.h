@@ -87,6 +87,36 @@ int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* 
 int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                int M, int N, int K, void* stream);
 
+/*
+ * Blocked scale layout -- the layout in which the block-scaled tensor-core MMA reads
+ * scale factors (through tcgen05.cp .32x128b.warpx4; "NVFP4 GEMM on Blackwell",
+ * "Tensor Cores and Tensor Memory"). For R rows and K columns (K % 64 == 0):
+ * rows are padded to a multiple of 128; block (rb, j) holds the scales of rows
+ * 128rb .. 128rb+127 for K elements 64j .. 64j+63 and is 512 contiguous bytes at
+ * offset (rb * K/64 + j) * 512; inside a block, the 16-byte line l (0 <= l < 32)
+ * holds, in order, the 4 scale bytes (16-element groups 0..3 of the 64-K step) of
+ * rows l, l+32, l+64 and l+96. Padding rows are zero. Total size:
+ * gemm_nvfp4_blocked_scale_bytes(R, K) = ceil(R/128) * 128 * K/16 bytes.
+ */
+long long gemm_nvfp4_blocked_scale_bytes(int rows, int K);   /* -1 if K % 64 != 0 or a size < 0 */
+
+/*
+ * gemm_nvfp4_pack_scales -- rearrange row-major scales SF[rows][K/16] (device) into
+ * the blocked layout at SF_blocked (device, gemm_nvfp4_blocked_scale_bytes(rows, K)
+ * bytes, caller-owned). One kernel launch on `stream`. Constraints: K % 64 == 0,
+ * ceil(rows/128) <= 65535, both pointers 16-byte aligned.
+ */
+int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, void* stream);
+
+/*
+ * gemm_nvfp4_blocked -- gemm_nvfp4 with SFA and SFB given in the blocked layout
+ * (gemm_nvfp4_blocked_scale_bytes(M, K) and (N, K) bytes). Same operands, result,
+ * constraints and errors as gemm_nvfp4. This is the fast path: a stage's scales for
+ * 128 rows are one contiguous 2 KB block, loaded by TMA together with the codes.
+ */
+int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                       int M, int N, int K, void* stream);
+
 /* Human-readable name of a gemm_status_t value (static string, never NULL). */
 const char* gemm_status_string(int status);
 
@@ -119,7 +149,9 @@ typedef struct {
     uint32_t wait_limit_us;   /* bound on each internal wait; 0 = default (2 s) */
     uint32_t debug_flags;     /* 0 in production; 1 = make the MMA issuer wait on a barrier
                                  nobody arrives on (exercises the timeout path) */
-    int reserved[4];     /* must be zero */
+    int no_tail_split;   /* 0: when the last wave of a persistent grid is at most half full,
+                            its tiles are computed as two N-halves each; 1: never */
+    int reserved[3];     /* must be zero */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
@@ -130,6 +162,10 @@ int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, voi
  * wait_limit_us and debug_flags apply; kernel must be GEMM_KERNEL_DEFAULT). */
 int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                   int M, int N, int K, void* stream, const gemm_options_t* options);
+
+/* gemm_nvfp4_blocked with explicit options (as for gemm_nvfp4_ex). */
+int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                          int M, int N, int K, void* stream, const gemm_options_t* options);
 
 /*
  * gemm_tile_coord -- host evaluation of the persistent tile order used by the

@@ -85,6 +85,27 @@ def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
     assert_bf16_close(C, oracle.gemm_bf16(A, B), K, f"kernel {kernel} clusters {max_clusters} group {group_m}")
 
 
+@pytest.mark.parametrize("max_clusters", [16, 9, 19])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+def test_tail_wave_split_into_halves(kernel, max_clusters):
+    """A last wave at most half full is computed as N-halves of its tiles (N = 128 MMAs)."""
+    M, N, K = 1280, 1000, 328     # 5 x 4 tiles (2-CTA) with a ragged last column block
+    A, B = si.bf16_problem(31, M, N, K)
+    ref = oracle.gemm_bf16(A, B)
+    split = run(A, B, kernel=kernel, max_clusters=max_clusters)
+    assert_bf16_close(split, ref, K, f"split, clusters {max_clusters}")
+    whole = run(A, B, kernel=kernel, max_clusters=max_clusters, no_tail_split=1)
+    assert_bf16_close(whole, ref, K, f"no split, clusters {max_clusters}")
+
+
+@pytest.mark.parametrize("shape", [(256, 256, 256), (200, 136, 64), (512, 512, 1024)], ids=lambda s: "x".join(map(str, s)))
+def test_small_problems_split_across_clusters(shape):
+    """Fewer tiles than half the co-resident clusters: every tile runs as two N-halves."""
+    M, N, K = shape
+    A, B = si.bf16_problem(0, M, N, K, kind="int")
+    assert_bf16_exact(run(A, B), oracle.gemm_bf16(A, B), f"{shape}")
+
+
 def test_integer_inputs_many_tiles_bit_exact():
     M, N, K = 1536, 1280, 1024
     A, B = si.bf16_problem(9, M, N, K, kind="int")

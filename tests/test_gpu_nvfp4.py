@@ -26,13 +26,48 @@ def setup():
     assert st == g.GEMM_OK, f"a kernel reported status {st} ({detail:#x})"
 
 
-def run(a, sfa, b, sfb, **opt):
-    C = g.matmul_nvfp4(a.to(DEV), sfa.to(DEV), b.to(DEV), sfb.to(DEV), opts=g.options(**opt) if opt else None)
+PATHS = ["rowmajor_scales", "blocked_scales"]
+
+
+def run(a, sfa, b, sfb, path="rowmajor_scales", **opt):
+    """GEMM through the C ABI; the blocked path packs the scales on the GPU first."""
+    opts = g.options(**opt) if opt else None
+    a, sfa, b, sfb = (t.to(DEV) for t in (a, sfa, b, sfb))
+    if path == "blocked_scales":
+        C = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb), opts=opts)
+    else:
+        C = g.matmul_nvfp4(a, sfa, b, sfb, opts=opts)
     torch.cuda.synchronize()
     return bits(C)
 
 
-def test_code_points_through_the_tensor_cores():
+def blocked_layout_reference(sf: np.ndarray, K: int) -> np.ndarray:
+    """The blocked scale layout written out from its definition in include/gemm.h."""
+    rows = sf.shape[0]
+    rb_count, ksteps = -(-rows // 128), K // 64
+    out = np.zeros(rb_count * 128 * (K // 16), dtype=np.uint8)
+    for rb in range(rb_count):
+        for j in range(ksteps):
+            base = (rb * ksteps + j) * 512
+            for l in range(32):
+                for q in range(4):
+                    r = rb * 128 + l + 32 * q
+                    if r < rows:
+                        out[base + 16 * l + 4 * q: base + 16 * l + 4 * q + 4] = sf[r, 4 * j: 4 * j + 4]
+    return out
+
+
+@pytest.mark.parametrize("rows,K", [(128, 64), (300, 512), (1, 1088), (256, 4096)])
+def test_pack_scales_layout(rows, K):
+    sf = si.e4m3_scales(7, si.TENSOR_SFA, rows, K // 16)
+    packed = g.pack_scales(sf.to(DEV))
+    torch.cuda.synchronize()
+    assert packed.numel() == g.nvfp4_blocked_scale_bytes(rows, K)
+    assert np.array_equal(packed.cpu().numpy(), blocked_layout_reference(sf.numpy(), K))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_code_points_through_the_tensor_cores(path):
     """Row 0 of A holds the 16 E2M1 codes (unit scales); B row j is one-hot at element j:
     C[0, j] must be code j's value, so the hardware's E2M1 decode matches the oracle's."""
     M, N, K = 256, 256, 256
@@ -42,13 +77,14 @@ def test_code_points_through_the_tensor_cores():
     onehot[torch.arange(16), torch.arange(16)] = 0x2           # 1.0
     sf = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8)
     a, b = si.pack_e2m1(codes), si.pack_e2m1(onehot)
-    got = oracle.bf16_bits_to_f64(run(a, sf, b, sf))
+    got = oracle.bf16_bits_to_f64(run(a, sf, b, sf, path))
     ref = oracle.gemm_nvfp4(a, sf, b, sf)
     assert list(got[0, :16]) == list(ref[0, :16])
     assert np.array_equal(got, ref)
 
 
-def test_scale_placement_per_row_and_block():
+@pytest.mark.parametrize("path", PATHS)
+def test_scale_placement_per_row_and_block(path):
     """Distinct power-of-two scales per (row, 16-block) on all-ones codes: C[i, j] is the exact
     dot product of the two scale rows, so a scale routed to the wrong row or block shows."""
     M, N, K = 256, 256, 512
@@ -57,41 +93,48 @@ def test_scale_placement_per_row_and_block():
     rng = np.random.default_rng(3)
     sfa = torch.from_numpy(rng.choice([0x30, 0x38, 0x40, 0x48], size=(M, K // 16)).astype(np.uint8))
     sfb = torch.from_numpy(rng.choice([0x28, 0x38, 0x40], size=(N, K // 16)).astype(np.uint8))
-    assert_bf16_exact(run(a, sfa, a, sfb), oracle.gemm_nvfp4(a, sfa, a, sfb), "scale placement")
+    assert_bf16_exact(run(a, sfa, a, sfb, path), oracle.gemm_nvfp4(a, sfa, a, sfb), "scale placement")
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 256), (512, 512, 1024), (300, 264, 512), (1, 8, 256), (640, 768, 2048)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_unit_scales_bit_exact(shape):
+@pytest.mark.parametrize("path", PATHS)
+def test_unit_scales_bit_exact(shape, path):
     """All scales 1.0: products are multiples of 1/4 and |sums| <= 36 K, exact in FP32."""
     M, N, K = shape
     a, _, b, _ = si.nvfp4_problem(11, M, N, K)
     sfa = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8)
     sfb = torch.full((N, K // 16), E4M3_ONE, dtype=torch.uint8)
-    assert_bf16_exact(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape}")
+    assert_bf16_exact(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape} {path}")
 
 
 @pytest.mark.parametrize("shape", [(256, 256, 256), (512, 512, 1024), (300, 264, 512), (1000, 776, 2304)],
                          ids=lambda s: "x".join(map(str, s)))
-def test_random_scales(shape):
+@pytest.mark.parametrize("path", PATHS)
+def test_random_scales(shape, path):
     """Codes uniform over the 16 code points, scales uniform over E4M3 values in [2^-4, 2^4]."""
     M, N, K = shape
     a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K)
-    assert_nvfp4_close(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape}")
+    assert_nvfp4_close(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape} {path}")
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 2), (5, 1)])
-def test_many_tiles_per_cluster(max_clusters, group_m):
-    M, N, K = 1280, 1024, 1280    # 5 x 4 tiles, 5 K stages: the 4-stage ring wraps inside a tile
+def test_many_tiles_per_cluster(max_clusters, group_m, path):
+    M, N, K = 1280, 1024, 1536    # 5 x 4 tiles, 6 K stages: the stage ring wraps inside a tile
     a, sfa, b, sfb = si.nvfp4_problem(21, M, N, K)
-    assert_nvfp4_close(run(a, sfa, b, sfb, max_clusters=max_clusters, group_m=group_m),
+    assert_nvfp4_close(run(a, sfa, b, sfb, path, max_clusters=max_clusters, group_m=group_m),
                        oracle.gemm_nvfp4(a, sfa, b, sfb), f"clusters {max_clusters}")
 
 
-def test_c5_8192_cubed_sampled():
+@pytest.mark.parametrize("path", PATHS)
+def test_c5_8192_cubed_sampled(path):
     M = N = K = 8192
     a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K, device=DEV)
-    C = g.matmul_nvfp4(a, sfa, b, sfb)
+    if path == "blocked_scales":
+        C = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb))
+    else:
+        C = g.matmul_nvfp4(a, sfa, b, sfb)
     torch.cuda.synchronize()
     rows, cols = sample_coords(M, N, 4096, 4)
     ref = oracle.gemm_nvfp4_at(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu(), rows, cols)
@@ -103,7 +146,7 @@ def test_c5_shape_unit_scales_sampled_bit_exact():
     M = N = K = 8192
     a, _, b, _ = si.nvfp4_problem(4, M, N, K, device=DEV)
     sfa = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8, device=DEV)
-    C = g.matmul_nvfp4(a, sfa, b, sfa)
+    C = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfa))
     torch.cuda.synchronize()
     rows, cols = sample_coords(M, N, 8192, 5)
     ref = oracle.gemm_nvfp4_at(a.cpu(), sfa.cpu(), b.cpu(), sfa.cpu(), rows, cols)
@@ -122,12 +165,17 @@ def test_empty_and_rejected():
     assert e.value.status == g.GEMM_ERR_UNSUPPORTED_SHAPE
 
 
-def test_bounded_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("path", PATHS)
+def test_bounded_wait_reports_timeout_and_context_survives(path):
     g.get_device_status()
     a, sfa, b, sfb = si.nvfp4_problem(4, 512, 512, 512, device=DEV)
-    g.matmul_nvfp4(a, sfa, b, sfb, opts=g.options(wait_limit_us=100_000, debug_flags=1))
+    opts = g.options(wait_limit_us=100_000, debug_flags=1)
+    if path == "blocked_scales":
+        g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb), opts=opts)
+    else:
+        g.matmul_nvfp4(a, sfa, b, sfb, opts=opts)
     st, _ = g.get_device_status()
     assert st == g.GEMM_ERR_TIMEOUT
     a, sfa, b, sfb = si.nvfp4_problem(5, 256, 256, 256)
-    assert_nvfp4_close(run(a, sfa, b, sfb), oracle.gemm_nvfp4(a, sfa, b, sfb), "after timeout")
+    assert_nvfp4_close(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), "after timeout")
     assert g.get_device_status()[0] == g.GEMM_OK
