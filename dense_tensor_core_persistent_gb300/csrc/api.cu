@@ -11,7 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 #include "host_common.h"
 #include "schedule.h"
 

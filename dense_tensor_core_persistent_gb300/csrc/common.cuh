@@ -43,6 +43,12 @@ __device__ __forceinline__ uint64_t umma_desc_plain(uint32_t smem_addr, uint32_t
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
+// Descriptor of the operand `bytes` further on (bytes % 16 == 0): the start address is the
+// low field, and shared-memory addresses stay below 2^18, so the field never overflows.
+__device__ __forceinline__ uint64_t umma_desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: BF16 x BF16 -> FP32, both operands K-major.
 // bits 4-5 D format (1 = F32), 7-9 A format (1 = BF16), 10-12 B format (1 = BF16),
 // 15/16 A/B major (0 = K), 17-22 N >> 3, 24-28 M >> 4.
@@ -70,9 +76,9 @@ static __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parit
                                              bool honour_abort) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    // suspended waits of at most 20 us, so the abort flag and the time limit are
+    // still checked often; a completed phase wakes the thread at once
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (honour_abort && *w.abort_flag) return false;
     if (globaltimer_ns() - t0 > w.limit_ns) {
       atomicCAS(w.status, 0u, code);

@@ -180,6 +180,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
       bool ok = true;
       if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
       int it = 0;
+      const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
+      uint64_t a_desc = a_desc0, b_desc = b_desc0;  // advanced with the ring position
       for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
         const uint32_t idesc = (i >= p.num_tiles - p.split_tiles) ? IDESC_HALF : IDESC_FULL;
         const uint32_t slot = static_cast<uint32_t>(it) & 1u;
@@ -196,12 +198,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
-          const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < L::BLOCK_K / L::UMMA_K; ++kk) {
             const uint32_t koff = kk * L::UMMA_K * 2;  // bytes inside the 128-byte swizzle row
-            mma_f16<CG>(d_tmem, umma_desc_sw128(sa + koff), umma_desc_sw128(sb + koff), idesc,
+            mma_f16<CG>(d_tmem, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
           }
           // Release the stage when these MMAs have read it; never wait here.
@@ -210,6 +210,11 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
+            a_desc = a_desc0;
+            b_desc = b_desc0;
+          } else {
+            a_desc = umma_desc_advance(a_desc, L::A_BYTES);
+            b_desc = umma_desc_advance(b_desc, L::B_BYTES);
           }
         }
         if (!ok) break;

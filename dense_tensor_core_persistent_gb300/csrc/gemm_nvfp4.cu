@@ -69,7 +69,12 @@ struct Nvfp4Layout {
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;
   static constexpr int SF_WARP = 2 + EPI_WARPS;            // warp 6 (row-major scales only)
-  static constexpr int NUM_THREADS = 32 * ((BLOCKED ? 2 : 3) + EPI_WARPS);
+  // Scale-copy warps (leader CTA): one thread issues a tcgen05.cp only every ~56 cycles,
+  // so the 12 copies of a stage are spread over 2 warps (copier c handles MMAs 2c, 2c+1:
+  // SFA and both SFB halves) and the MMA thread issues only MMAs.
+  static constexpr int COPY_WARPS = 2;
+  static constexpr int COPY_WARP0 = SF_WARP + (BLOCKED ? 0 : 1);
+  static constexpr int NUM_THREADS = 32 * (COPY_WARP0 + COPY_WARPS);
   static constexpr int LAND_STAGES = BLOCKED ? 0 : STAGES;
 
   static constexpr int OFF_A = 0;
@@ -80,8 +85,8 @@ struct Nvfp4Layout {
   static constexpr int OFF_SFB_IN = OFF_SFA_IN + LAND_STAGES * SFA_BYTES;
   static constexpr int OFF_EPI = OFF_SFB_IN + LAND_STAGES * SFB_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // full[S], empty[S], sf_landed[S], sf_full[S], tmem_full, tmem_empty, never, drain
-  static constexpr int NUM_BARS = 4 * STAGES + 4;
+  // full[S], empty[S], sf_landed[S], sf_full[S], sf_ready[S], tmem_full, tmem_empty, never, drain
+  static constexpr int NUM_BARS = 5 * STAGES + 4;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
@@ -129,7 +134,8 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
   const uint32_t bar_empty = bar_full + 8 * STAGES;     // stage consumed by the MMAs (both CTAs)
   const uint32_t bar_sfland = bar_empty + 8 * STAGES;   // scale TMA landed (each CTA's own)
   const uint32_t bar_sffull = bar_sfland + 8 * STAGES;  // rearranged scales ready (leader's, 2 arrivals)
-  const uint32_t bar_tfull = bar_sffull + 8 * STAGES;   // accumulator ready
+  const uint32_t bar_sfready = bar_sffull + 8 * STAGES; // scales copied to TMEM (leader's, 3 commits)
+  const uint32_t bar_tfull = bar_sfready + 8 * STAGES;  // accumulator ready
   const uint32_t bar_tempty = bar_tfull + 8;            // accumulator drained (leader's, 8 arrivals)
   const uint32_t bar_never = bar_tempty + 8;
   const uint32_t bar_drain = bar_never + 8;
@@ -143,6 +149,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
       mbar_init(bar_empty + 8 * s, 1);
       mbar_init(bar_sfland + 8 * s, 1);
       mbar_init(bar_sffull + 8 * s, L::CG);
+      mbar_init(bar_sfready + 8 * s, L::COPY_WARPS);
     }
     mbar_init(bar_tfull, 1);
     mbar_init(bar_tempty, L::EPI_WARPS * L::CG);
@@ -252,6 +259,52 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
     }
     if (!ok) settle_after_abort();
     __syncwarp();
+  } else if (warp >= L::COPY_WARP0) {
+    // ------------------------------------------------------------ scale copiers (leader)
+    // Copier c moves, for every stage, the scale blocks of MMAs 2c and 2c+1 (SFA, SFB rows
+    // 0-127, SFB rows 128-255: 6 copies) from shared memory to the stage's TMEM scale
+    // slot, then commits to sf_ready. Waiting for
+    // the stage's data (full / sf_full) also guarantees the MMAs STAGES stages earlier,
+    // which read the same TMEM slot, have completed (the data could not be reloaded before).
+    const int c = static_cast<int>(warp) - L::COPY_WARP0;
+    if (rank == 0 && lane == 0) {
+      const int my_tiles = (p.num_tiles - cluster_idx + num_clusters - 1) / num_clusters;
+      const long long total = static_cast<long long>(my_tiles > 0 ? my_tiles : 0) * p.k_iters;
+      const uint32_t data_bar = BLOCKED ? bar_full : bar_sffull;
+      const uint64_t sfa0 = umma_desc_plain(base + L::OFF_SFA, 128), sfb0 = umma_desc_plain(base + L::OFF_SFB, 128);
+      uint64_t sfa = sfa0, sfb = sfb0;
+      uint32_t col = tmem_base + L::SF_TMEM_COL0;
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (long long g = 0; g < total; ++g) {
+        if (!wait_phase(data_bar + 8 * stage, phase, wctx, status_code(kRoleScales, 0x300 + stage))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int jj = 0; jj < L::KSTEPS / L::COPY_WARPS; ++jj) {
+          const uint32_t j = c * (L::KSTEPS / L::COPY_WARPS) + jj;
+          tmem_cp_32x128b_warpx4<2>(col + 4 * j, umma_desc_advance(sfa, j * L::SF_BLOCK));
+          tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * j, umma_desc_advance(sfb, j * L::SF_BLOCK));
+          tmem_cp_32x128b_warpx4<2>(col + 20 + 8 * j, umma_desc_advance(sfb, 2048 + j * L::SF_BLOCK));
+        }
+        mma_commit_pair_multicast(bar_sfready + 8 * stage, 0x1);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+          sfa = sfa0;
+          sfb = sfb0;
+          col = tmem_base + L::SF_TMEM_COL0;
+        } else {
+          sfa = umma_desc_advance(sfa, L::SFA_BYTES);
+          sfb = umma_desc_advance(sfb, L::SFB_BYTES);
+          col += L::SF_COLS;
+        }
+      }
+      if (!ok) settle_after_abort();
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
     if (rank == 0 && lane == 0) {
@@ -260,6 +313,12 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
       bool ok = true;
       if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
       int it = 0;
+      // Per-stage operand descriptors and scale columns, advanced with the ring position
+      // instead of being rebuilt from addresses for every instruction.
+      const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
+      const uint32_t sf_col0 = tmem_base + L::SF_TMEM_COL0;
+      uint64_t a_desc = a_desc0, b_desc = b_desc0;
+      uint32_t sf_col = sf_col0;
       for (int t = cluster_idx; t < p.num_tiles && ok; t += num_clusters, ++it) {
         if (!wait_phase(bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u, wctx, status_code(kRoleMma, 0x100))) {
           ok = false;
@@ -267,51 +326,30 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES, BLOCKED>::NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         for (int kb = 0; kb < p.k_iters; ++kb) {
-          const uint32_t sf_col = tmem_base + L::SF_TMEM_COL0 + stage * L::SF_COLS;
-          // scales first: they are small and usually land before the tiles (in blocked
-          // mode they travel with the tiles and the full barrier covers them)
-          if (!BLOCKED) {
-            if (!wait_phase(bar_sffull + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-          } else {
-            if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
+          // the stage's scales are in TMEM (copy warps) and its tiles in shared memory
+          if (!wait_phase(bar_sfready + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage)) ||
+              !wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
+            ok = false;
+            break;
           }
-          const uint32_t sfa_src = base + L::OFF_SFA + stage * L::SFA_BYTES;
-          const uint32_t sfb_src = base + L::OFF_SFB + stage * L::SFB_BYTES;
-#pragma unroll
-          for (int j = 0; j < L::KSTEPS; ++j) {
-            tmem_cp_32x128b_warpx4<2>(sf_col + 4 * j, umma_desc_plain(sfa_src + j * L::SF_BLOCK, 128));
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tmem_cp_32x128b_warpx4<2>(sf_col + 16 + 8 * j + 4 * h,
-                                        umma_desc_plain(sfb_src + h * 2048 + j * L::SF_BLOCK, 128));
-          }
-          if (!BLOCKED) {
-            if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after_sync();
-          }
-          const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
-          const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
+          tc_fence_after_sync();
 #pragma unroll
           for (int j = 0; j < L::KSTEPS; ++j) {
             const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
-            mma_nvf4<2>(tmem_base, umma_desc_sw128(sa + koff), umma_desc_sw128(sb + koff), IDESC, sf_col + 4 * j,
-                        sf_col + 16 + 8 * j, (kb | j) != 0 ? 1u : 0u);
+            mma_nvf4<2>(tmem_base, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), IDESC,
+                        sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) != 0 ? 1u : 0u);
           }
           mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
+            a_desc = a_desc0;
+            b_desc = b_desc0;
+            sf_col = sf_col0;
+          } else {
+            a_desc = umma_desc_advance(a_desc, L::A_BYTES);
+            b_desc = umma_desc_advance(b_desc, L::B_BYTES);
+            sf_col += L::SF_COLS;
           }
         }
         if (!ok) break;

@@ -6,7 +6,7 @@
 
 #include <cstdint>
 
-#include "../../include/gemm.h"
+#include "gemm.h"
 
 namespace dtcp {
 

@@ -89,6 +89,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same, but lets the hardware suspend the thread for up to `suspend_ns` while the phase
+// is incomplete (the thread resumes as soon as the phase completes). A suspended thread
+// takes no issue slots from the warps it shares a scheduler with.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- TMA (bulk tensor copies)
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
