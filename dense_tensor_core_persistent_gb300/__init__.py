@@ -26,6 +26,7 @@ GEMM_ERR_ARCH = 5
 GEMM_ERR_DRIVER = 6
 GEMM_ERR_LAUNCH = 7
 GEMM_ERR_TIMEOUT = 8
+GEMM_ERR_OUT_OF_MEMORY = 9
 
 GEMM_KERNEL_DEFAULT = 0
 GEMM_KERNEL_BF16_1CTA = 1

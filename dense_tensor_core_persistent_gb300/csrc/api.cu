@@ -172,6 +172,34 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   return GEMM_OK;
 }
 
+static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// A stream-ordered memory pool owned by the library, one per device, for the temporary
+// blocked-scale workspace of gemm_nvfp4. Freed blocks stay in the pool (release threshold
+// at the maximum), so after the first calls the workspace costs no allocation from the
+// driver; blocks freed on one stream are reused by later work on any stream in order.
+static cudaMemPool_t workspace_pool(int device) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[64] = {nullptr};
+  if (device < 0 || device >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pools[device] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[device] = pool;
+  }
+  return pools[device];
+}
+
 // C = 0 for an empty K (the sum over no terms); BF16 zero is the all-zero bit pattern.
 static int zero_output(void* C, int M, int N, cudaStream_t stream) {
   if (cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * 2, stream) != cudaSuccess) {
@@ -218,14 +246,31 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   if (M == 0 || N == 0) return GEMM_OK;
   if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr || SFA == nullptr || SFB == nullptr)))
     return GEMM_ERR_INVALID_ARG;
-  if (K % 256 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
+  if (K % 256 != 0 || N % 8 != 0 || ceil_div(M, 128) > 65535 || ceil_div(N, 128) > 65535)
+    return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))))
     return GEMM_ERR_MISALIGNED;
   int device = 0, err = 0;
   if (current_device_info(&device, &err) == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return zero_output(C, M, N, s);
-  return run_gemm_nvfp4(A, SFA, B, SFB, C, M, N, K, s, opt, false);
+  // Rearrange both scale matrices into the blocked layout in a stream-ordered workspace,
+  // run the blocked GEMM, and free the workspace in stream order behind it.
+  const size_t bytes_a = round_up(static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(M, K)), 256);
+  const size_t bytes_b = static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(N, K));
+  cudaMemPool_t pool = workspace_pool(device);
+  void* ws = nullptr;
+  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b, pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_OUT_OF_MEMORY;
+  }
+  uint8_t* sfa_blk = static_cast<uint8_t*>(ws);
+  uint8_t* sfb_blk = sfa_blk + bytes_a;
+  st = run_pack_scales(SFA, sfa_blk, M, K, s);
+  if (st == GEMM_OK) st = run_pack_scales(SFB, sfb_blk, N, K, s);
+  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, sfa_blk, B, sfb_blk, C, M, N, K, s, opt);
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
+  return st;
 }
 
 int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
@@ -267,7 +312,7 @@ int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B,
   if (current_device_info(&device, &err) == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return zero_output(C, M, N, s);
-  return run_gemm_nvfp4(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt, true);
+  return run_gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt);
 }
 
 int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C, int M,
@@ -286,6 +331,7 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_DRIVER: return "tensor map encoding failed";
     case GEMM_ERR_LAUNCH: return "kernel launch failed";
     case GEMM_ERR_TIMEOUT: return "device wait timed out";
+    case GEMM_ERR_OUT_OF_MEMORY: return "out of device memory for the scale workspace";
     default: return "unknown status";
   }
 }

@@ -45,8 +45,8 @@ struct RunOptions {
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt);
-int run_gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
-                   cudaStream_t stream, const RunOptions& opt, bool blocked_scales);
+int run_gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                           int M, int N, int K, cudaStream_t stream, const RunOptions& opt);
 int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).

@@ -22,9 +22,12 @@
  *   - `stream` is a cudaStream_t / CUstream handle (NULL = legacy default
  *     stream). Calls are asynchronous: they enqueue work and return; nothing
  *     is synchronised. Results are visible to later work on `stream`.
- *   - The library allocates no device memory. It holds one process-wide
- *     device status word (a static __device__ variable) that kernels set if a
- *     bounded internal wait expires; read it with gemm_get_device_status.
+ *   - Device memory: gemm_bf16, gemm_nvfp4_blocked and gemm_nvfp4_pack_scales
+ *     allocate nothing. gemm_nvfp4 takes a temporary workspace for the
+ *     rearranged scales from a library-owned, stream-ordered memory pool (see
+ *     gemm_nvfp4). The library also holds one process-wide device status word
+ *     (a static __device__ variable) that kernels set if a bounded internal
+ *     wait expires; read it with gemm_get_device_status.
  *   - Return value: GEMM_OK (0) or a gemm_status_t code for problems found on
  *     the host before launch. Nothing is launched when an error is returned.
  *     Faults during execution surface through the stream like any CUDA error.
@@ -49,7 +52,8 @@ typedef enum {
     GEMM_ERR_ARCH = 5,              /* current device is not compute capability 10.3 (sm_103) */
     GEMM_ERR_DRIVER = 6,            /* cuTensorMapEncodeTiled unavailable or rejected the operand */
     GEMM_ERR_LAUNCH = 7,            /* the kernel launch itself failed */
-    GEMM_ERR_TIMEOUT = 8            /* device side: a bounded wait inside a kernel expired */
+    GEMM_ERR_TIMEOUT = 8,           /* device side: a bounded wait inside a kernel expired */
+    GEMM_ERR_OUT_OF_MEMORY = 9      /* gemm_nvfp4 could not obtain its scale workspace */
 } gemm_status_t;
 
 /*
@@ -79,10 +83,17 @@ int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* 
  *        16q .. 16q+15 of row m at SFA[m][q]. SFB: N x K/16 bytes, same.
  *   C:   M x N BF16, row stride N.
  * Constraints: M, N, K >= 0; K % 256 == 0 (one 128-byte swizzle row of codes
- * and a 16-byte row of scales per pipeline stage); N % 8 == 0; all pointers
- * 16-byte aligned. Ragged M / N as for gemm_bf16. K == 0 sets C to zero.
+ * per pipeline stage); N % 8 == 0; ceil(M/128), ceil(N/128) <= 65535; all
+ * pointers 16-byte aligned. Ragged M / N as for gemm_bf16. K == 0 sets C to zero.
  * Scales are used as the hardware's unsigned E4M3 (UE4M3): the sign bit of a
  * scale byte must be 0; NaN scales give unspecified results.
+ * Launches: two gemm_nvfp4_pack_scales kernels (SFA, SFB) into a workspace of
+ * gemm_nvfp4_blocked_scale_bytes(M, K) + gemm_nvfp4_blocked_scale_bytes(N, K)
+ * bytes (+ up to 255 bytes of alignment), then the gemm_nvfp4_blocked kernel. The
+ * workspace comes from a library-owned stream-ordered pool (cudaMallocFromPoolAsync)
+ * and is returned to it in stream order after the GEMM, so concurrent calls on
+ * different streams use different workspaces. Returns GEMM_ERR_OUT_OF_MEMORY if
+ * the workspace cannot be obtained.
  */
 int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                int M, int N, int K, void* stream);
@@ -159,7 +170,8 @@ int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, voi
                  const gemm_options_t* options);
 
 /* gemm_nvfp4 with explicit options (only persistent, group_m, max_clusters,
- * wait_limit_us and debug_flags apply; kernel must be GEMM_KERNEL_DEFAULT). */
+ * wait_limit_us, debug_flags and no_tail_split apply; kernel must be
+ * GEMM_KERNEL_DEFAULT). */
 int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                   int M, int N, int K, void* stream, const gemm_options_t* options);
 

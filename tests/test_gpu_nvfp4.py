@@ -179,3 +179,20 @@ def test_bounded_wait_reports_timeout_and_context_survives(path):
     a, sfa, b, sfb = si.nvfp4_problem(5, 256, 256, 256)
     assert_nvfp4_close(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), "after timeout")
     assert g.get_device_status()[0] == g.GEMM_OK
+
+
+def test_concurrent_calls_on_two_streams_use_separate_workspaces():
+    """gemm_nvfp4 (row-major scales) takes its scale workspace from a stream-ordered pool:
+    two calls in flight on different streams must not share it."""
+    M, N, K = 512, 512, 2048
+    probs = [si.nvfp4_problem(40 + i, M, N, K, device=DEV) for i in range(2)]
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(2)]
+    streams = [torch.cuda.Stream(device=DEV) for _ in range(2)]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for (a, sfa, b, sfb), out, s in zip(probs, outs, streams):
+            g.gemm_nvfp4(a, sfa, b, sfb, out, M, N, K, stream=s)
+    torch.cuda.synchronize()
+    for (a, sfa, b, sfb), out in zip(probs, outs):
+        ref = oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu())
+        assert_nvfp4_close(bits(out), ref, "two streams")
