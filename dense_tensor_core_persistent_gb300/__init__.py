@@ -27,6 +27,8 @@ GEMM_ERR_DRIVER = 6
 GEMM_ERR_LAUNCH = 7
 GEMM_ERR_TIMEOUT = 8
 GEMM_ERR_OUT_OF_MEMORY = 9
+GEMM_ERR_SCRATCH_TOO_SMALL = 10
+NVFP4_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 GEMM_KERNEL_DEFAULT = 0
 GEMM_KERNEL_BF16_1CTA = 1
@@ -37,6 +39,7 @@ EXPORTS = (
     "gemm_bf16", "gemm_nvfp4", "gemm_status_string", "gemm_get_device_status", "gemm_bf16_ex",
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
+    "gemm_nvfp4_noalloc",
 )
 
 
@@ -101,6 +104,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_nvfp4_blocked.restype = I
         l.gemm_nvfp4_blocked_ex.argtypes = [P, P, P, P, P, I, I, I, P, ctypes.POINTER(gemm_options_t)]
         l.gemm_nvfp4_blocked_ex.restype = I
+        l.gemm_nvfp4_noalloc.argtypes = [P, P, P, P, P, I, I, I, P]
+        l.gemm_nvfp4_noalloc.restype = I
         l.gemm_launch_count.argtypes = []
         l.gemm_launch_count.restype = ctypes.c_ulonglong
         _lib = l
@@ -181,6 +186,14 @@ def gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M: int, N: int, K: int
         st = l.gemm_nvfp4_blocked_ex(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
                                      _stream(stream), ctypes.byref(opts))
     _check(st, "gemm_nvfp4_blocked")
+
+
+def gemm_nvfp4_noalloc(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None) -> None:
+    """gemm_nvfp4 without any device allocation: the rearranged scales live in a fixed
+    16 MiB array inside the library (see include/gemm.h for the size limit and the
+    rule that calls overlapping on the GPU must be ordered)."""
+    _check(lib().gemm_nvfp4_noalloc(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _stream(stream)),
+           "gemm_nvfp4_noalloc")
 
 
 def get_device_status(stream=None) -> tuple[int, int]:

@@ -332,6 +332,8 @@ const char* gemm_status_string(int status) {
     case GEMM_ERR_LAUNCH: return "kernel launch failed";
     case GEMM_ERR_TIMEOUT: return "device wait timed out";
     case GEMM_ERR_OUT_OF_MEMORY: return "out of device memory for the scale workspace";
+    case GEMM_ERR_SCRATCH_TOO_SMALL:
+      return "problem's rearranged scales exceed the fixed no-allocation scratch array (16 MiB)";
     default: return "unknown status";
   }
 }

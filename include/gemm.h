@@ -37,6 +37,7 @@
 #ifndef DTCP_GEMM_H
 #define DTCP_GEMM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -53,7 +54,9 @@ typedef enum {
     GEMM_ERR_DRIVER = 6,            /* cuTensorMapEncodeTiled unavailable or rejected the operand */
     GEMM_ERR_LAUNCH = 7,            /* the kernel launch itself failed */
     GEMM_ERR_TIMEOUT = 8,           /* device side: a bounded wait inside a kernel expired */
-    GEMM_ERR_OUT_OF_MEMORY = 9      /* gemm_nvfp4 could not obtain its scale workspace */
+    GEMM_ERR_OUT_OF_MEMORY = 9,     /* gemm_nvfp4 could not obtain its scale workspace */
+    GEMM_ERR_SCRATCH_TOO_SMALL = 10 /* gemm_nvfp4_noalloc: the problem's rearranged scales
+                                       exceed its fixed scratch array */
 } gemm_status_t;
 
 /*
@@ -126,6 +129,39 @@ int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, vo
  * 128 rows are one contiguous 2 KB block, loaded by TMA together with the codes.
  */
 int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                       int M, int N, int K, void* stream);
+
+/*
+ * gemm_nvfp4_noalloc -- gemm_nvfp4 for callers that must not let the library allocate
+ * device memory. (Not from the NVFP4 page: it has no counterpart there; it exists for
+ * callers of this library.)
+ *
+ * gemm_nvfp4 rearranges the row-major scales into the blocked layout in a workspace it
+ * takes from a memory pool. Some callers cannot allow that: code running where the CUDA
+ * allocator must not be entered (inside a custom allocator or memory manager, an error
+ * path, a loop with hard latency limits), or applications that account for every byte of
+ * device memory through their own allocator. This entry point uses instead a fixed
+ * scratch array compiled into the library: GEMM_NVFP4_NOALLOC_SCRATCH_BYTES (16 MiB) of
+ * device memory on every GPU that loads the library, held until the process exits.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Operands, layouts, result, constraints and errors are those of gemm_nvfp4, plus:
+ *   - the problem must satisfy
+ *       round_up(gemm_nvfp4_blocked_scale_bytes(M, K), 256) + gemm_nvfp4_blocked_scale_bytes(N, K)
+ *         <= GEMM_NVFP4_NOALLOC_SCRATCH_BYTES
+ *     (e.g. M = N = 8192 allows K up to 16384); larger problems return
+ *     GEMM_ERR_SCRATCH_TOO_SMALL and launch nothing;
+ *   - the first call on a device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ *     call before any stream capture;
+ *   - every call on a device uses the same scratch array, which keeps the last call's
+ *     contents (each call rewrites all of the part it reads, so nothing needs clearing).
+ *     Calls whose work overlaps on the GPU -- on different streams without ordering
+ *     between them -- race on it: order them on one stream or with events.
+ * Launches: two scale-packing kernels and the gemm_nvfp4_blocked kernel, on `stream`.
+ */
+#define GEMM_NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                        int M, int N, int K, void* stream);
 
 /* Human-readable name of a gemm_status_t value (static string, never NULL). */
