@@ -246,7 +246,7 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   if (M == 0 || N == 0) return GEMM_OK;
   if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr || SFA == nullptr || SFB == nullptr)))
     return GEMM_ERR_INVALID_ARG;
-  if (K % 256 != 0 || N % 8 != 0 || ceil_div(M, 128) > 65535 || ceil_div(N, 128) > 65535)
+  if (K % 256 != 0 || N % 8 != 0 || ceil_div(M, 128) + ceil_div(N, 128) > 65535)
     return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))))
     return GEMM_ERR_MISALIGNED;
@@ -266,8 +266,7 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   }
   uint8_t* sfa_blk = static_cast<uint8_t*>(ws);
   uint8_t* sfb_blk = sfa_blk + bytes_a;
-  st = run_pack_scales(SFA, sfa_blk, M, K, s);
-  if (st == GEMM_OK) st = run_pack_scales(SFB, sfb_blk, N, K, s);
+  st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s);
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, sfa_blk, B, sfb_blk, C, M, N, K, s, opt);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;

@@ -262,9 +262,9 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         for (int kb = 0; kb < p.k_iters; ++kb) {
-          // the stage's scales are in TMEM (copiers) and its tiles in shared memory
-          if (!wait_phase(bar_sfready + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage)) ||
-              !wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
+          // The stage's scales are in TMEM. The copiers copied them only after the stage's
+          // full barrier completed, so its tiles are in shared memory too.
+          if (!wait_phase(bar_sfready + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage))) {
             ok = false;
             break;
           }

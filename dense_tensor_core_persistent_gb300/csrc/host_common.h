@@ -48,6 +48,9 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
 int run_gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                            int M, int N, int K, cudaStream_t stream, const RunOptions& opt);
 int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream);
+// Both matrices of a GEMM in one launch (rows0 + rows1 row blocks).
+int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
+                     cudaStream_t stream);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).
 int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,

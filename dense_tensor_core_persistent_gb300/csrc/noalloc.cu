@@ -60,7 +60,7 @@ extern "C" int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B,
   if (M == 0 || N == 0) return GEMM_OK;
   if (C == nullptr || (K > 0 && (A == nullptr || B == nullptr || SFA == nullptr || SFB == nullptr)))
     return GEMM_ERR_INVALID_ARG;
-  if (K % 256 != 0 || N % 8 != 0 || ceil_div(M, 128) > 65535 || ceil_div(N, 128) > 65535)
+  if (K % 256 != 0 || N % 8 != 0 || ceil_div(M, 128) + ceil_div(N, 128) > 65535)
     return GEMM_ERR_UNSUPPORTED_SHAPE;
   if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 ||
       (K > 0 && ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(SFA) |
@@ -84,8 +84,7 @@ extern "C" int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B,
   if (scratch == nullptr) return GEMM_ERR_NO_DEVICE;
   // The pack kernel writes every byte the GEMM reads (padding rows as zeros), so nothing
   // left in the array by an earlier call needs clearing.
-  int st = run_pack_scales(SFA, scratch, M, K, s);
-  if (st == GEMM_OK) st = run_pack_scales(SFB, scratch + bytes_a, N, K, s);
+  int st = run_pack_scales2(SFA, scratch, M, SFB, scratch + bytes_a, N, K, s);
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, scratch, B, scratch + bytes_a, C, M, N, K, s, RunOptions());
   return st;
 }

@@ -26,12 +26,20 @@ constexpr int kPackRows = 128;    // one row block per CTA
 constexpr int kPackSteps = 16;    // 64-K steps per CTA (64 scale bytes per row)
 constexpr int kPackThreads = 256;
 
-// CTA (x, y): row block y, K steps 16 x .. 16 x + 15.
-__global__ void __launch_bounds__(kPackThreads) pack_scales_kernel(const uint8_t* __restrict__ sf,
-                                                                   uint8_t* __restrict__ out, int rows,
+// CTA (x, y): K steps 16 x .. 16 x + 15 of row block y of the first matrix, or of row
+// block y - rb0 of the second one (two matrices in one launch).
+__global__ void __launch_bounds__(kPackThreads) pack_scales_kernel(const uint8_t* __restrict__ sf0,
+                                                                   uint8_t* __restrict__ out0, int rows0,
+                                                                   const uint8_t* __restrict__ sf1,
+                                                                   uint8_t* __restrict__ out1, int rows1,
                                                                    int row_bytes, int ksteps) {
   __shared__ uint32_t tile[kPackRows][kPackSteps + 1];  // +1 word: conflict-free column reads
-  const int rb = blockIdx.y;
+  const int rb0 = (rows0 + kPackRows - 1) / kPackRows;
+  const bool second = static_cast<int>(blockIdx.y) >= rb0;
+  const uint8_t* __restrict__ sf = second ? sf1 : sf0;
+  uint8_t* __restrict__ out = second ? out1 : out0;
+  const int rows = second ? rows1 : rows0;
+  const int rb = second ? static_cast<int>(blockIdx.y) - rb0 : static_cast<int>(blockIdx.y);
   const int j0 = blockIdx.x * kPackSteps;
   const int nj = min(kPackSteps, ksteps - j0);
   for (int i = threadIdx.x; i < kPackRows * kPackSteps; i += kPackThreads) {
@@ -51,14 +59,21 @@ __global__ void __launch_bounds__(kPackThreads) pack_scales_kernel(const uint8_t
   }
 }
 
-int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream) {
+int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
+                     cudaStream_t stream) {
   const int ksteps = K / 64;
-  const dim3 grid(static_cast<unsigned>(ceil_div(ksteps, kPackSteps)), static_cast<unsigned>(ceil_div(rows, kPackRows)));
-  pack_scales_kernel<<<grid, kPackThreads, 0, stream>>>(static_cast<const uint8_t*>(SF),
-                                                        static_cast<uint8_t*>(SF_blocked), rows, K / 16, ksteps);
+  const int blocks_y = ceil_div(rows0, kPackRows) + ceil_div(rows1, kPackRows);
+  const dim3 grid(static_cast<unsigned>(ceil_div(ksteps, kPackSteps)), static_cast<unsigned>(blocks_y));
+  pack_scales_kernel<<<grid, kPackThreads, 0, stream>>>(static_cast<const uint8_t*>(SF0), static_cast<uint8_t*>(out0),
+                                                        rows0, static_cast<const uint8_t*>(SF1),
+                                                        static_cast<uint8_t*>(out1), rows1, K / 16, ksteps);
   if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
   count_launch();
   return GEMM_OK;
+}
+
+int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream) {
+  return run_pack_scales2(SF, SF_blocked, rows, nullptr, nullptr, 0, K, stream);
 }
 
 }  // namespace dtcp

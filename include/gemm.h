@@ -86,11 +86,11 @@ int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* 
  *        16q .. 16q+15 of row m at SFA[m][q]. SFB: N x K/16 bytes, same.
  *   C:   M x N BF16, row stride N.
  * Constraints: M, N, K >= 0; K % 256 == 0 (one 128-byte swizzle row of codes
- * per pipeline stage); N % 8 == 0; ceil(M/128), ceil(N/128) <= 65535; all
+ * per pipeline stage); N % 8 == 0; ceil(M/128) + ceil(N/128) <= 65535; all
  * pointers 16-byte aligned. Ragged M / N as for gemm_bf16. K == 0 sets C to zero.
  * Scales are used as the hardware's unsigned E4M3 (UE4M3): the sign bit of a
  * scale byte must be 0; NaN scales give unspecified results.
- * Launches: two gemm_nvfp4_pack_scales kernels (SFA, SFB) into a workspace of
+ * Launches: one scale-packing kernel (SFA and SFB together) into a workspace of
  * gemm_nvfp4_blocked_scale_bytes(M, K) + gemm_nvfp4_blocked_scale_bytes(N, K)
  * bytes (+ up to 255 bytes of alignment), then the gemm_nvfp4_blocked kernel. The
  * workspace comes from a library-owned stream-ordered pool (cudaMallocFromPoolAsync)
@@ -158,7 +158,8 @@ int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, co
  *     contents (each call rewrites all of the part it reads, so nothing needs clearing).
  *     Calls whose work overlaps on the GPU -- on different streams without ordering
  *     between them -- race on it: order them on one stream or with events.
- * Launches: two scale-packing kernels and the gemm_nvfp4_blocked kernel, on `stream`.
+ * Launches: one scale-packing kernel (SFA and SFB together) and the gemm_nvfp4_blocked
+ * kernel, on `stream`.
  */
 #define GEMM_NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B, const void* SFB, void* C,

@@ -196,3 +196,21 @@ def test_concurrent_calls_on_two_streams_use_separate_workspaces():
     for (a, sfa, b, sfb), out in zip(probs, outs):
         ref = oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu())
         assert_nvfp4_close(bits(out), ref, "two streams")
+
+
+def test_launches_per_call():
+    """gemm_nvfp4: one packing kernel for both scale matrices, then the GEMM kernel;
+    gemm_nvfp4_blocked: the GEMM kernel alone."""
+    M, N, K = 384, 264, 512
+    a, sfa, b, sfb = si.nvfp4_problem(6, M, N, K, device=DEV)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    before = g.launch_count()
+    g.gemm_nvfp4(a, sfa, b, sfb, C, M, N, K)
+    torch.cuda.synchronize()
+    assert g.launch_count() == before + 2
+    pa, pb = g.pack_scales(sfa), g.pack_scales(sfb)
+    torch.cuda.synchronize()
+    before = g.launch_count()
+    g.gemm_nvfp4_blocked(a, pa, b, pb, C, M, N, K)
+    torch.cuda.synchronize()
+    assert g.launch_count() == before + 1

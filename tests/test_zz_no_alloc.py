@@ -37,8 +37,10 @@ def _both(seed, M, N, K):
     want = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
     got = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
     g.gemm_nvfp4(a, sfa, b, sfb, want, M, N, K)
+    before = g.launch_count()
     g.gemm_nvfp4_noalloc(a, sfa, b, sfb, got, M, N, K)
     torch.cuda.synchronize()
+    assert g.launch_count() == before + 2  # scale packing (SFA and SFB together), GEMM
     return bits(got), want.cpu().double().numpy()
 
 
