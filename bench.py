@@ -447,7 +447,8 @@ def run_ours(args, cfg, world, rank, local):
         "config": {
             "workload": cfg["workload"], "M": M, "N": N, "K": K,
             "l2_flush": f"rotation over {R} input sets of {sb / 2**20:.0f} MiB (> 2x L2 = {2 * l2 / 2**20:.0f} MiB)",
-            "kernel": {0: "default (2-CTA persistent)", 1: "1-CTA", 2: "2-CTA"}[args.kernel]
+            "kernel": {0: "default (2-CTA persistent, 128-K stages)", 1: "1-CTA", 2: "2-CTA, 128-K stages",
+                       3: "2-CTA, 64-K stages"}[args.kernel]
             + ("" if not args.no_persistent else ", one tile per cluster")
             + (", no tail split" if args.no_tail_split else ""),
             "scales": (None if cfg["kind"] == "bf16" else

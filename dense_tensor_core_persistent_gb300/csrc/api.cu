@@ -123,6 +123,20 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }
 
+int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
+                   const uint64_t strides_bytes[2], const uint32_t box[3]) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_DRIVER;
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t b[3] = {box[0], box[1], box[2]};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, b, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
+}
+
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // ---------------------------------------------------------------- tile order
@@ -158,7 +172,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   for (int i = 0; i < 3; ++i)
     if (o->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
-  if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA) return GEMM_ERR_INVALID_ARG;
+  if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
   if (o->debug_flags & ~1u) return GEMM_ERR_INVALID_ARG;

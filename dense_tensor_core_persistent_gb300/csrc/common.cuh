@@ -96,6 +96,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   return wait_phase_slow(bar, parity, w, code, true);
 }
 
+// Same wait with the slow path inlined: for code that runs under a changed register
+// limit (setmaxnreg), where a call to an out-of-line function is not allowed to follow
+// the caller's register budget.
+__device__ __forceinline__ bool wait_phase_inline(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      atomicCAS(w.status, 0u, code);
+      *w.abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
 // Warp-collective form: every lane waits (so every lane acquires what the barrier
 // guards), and the outcome is made uniform so the warp leaves its loop together.
 __device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {

@@ -10,6 +10,10 @@
 //         barrier counts the bytes of both CTAs, and MMA completion is multicast to both.
 // The TMEM accumulator is double buffered (2 x 256 columns): the epilogue of tile i
 // drains one slot while the MMAs of tile i+1 fill the other.
+// A stage holds ATOMS columns of 64 K (one 128-byte swizzle row each). The default pair
+// kernel uses 3 stages of 128 K, 8 MMAs per barrier wait: the issuing thread spends about
+// 230 cycles per stage on the wait, fence and commit besides ~60 per MMA, so with 4 MMAs
+// (512 pipe cycles) per stage it can barely keep the tensor pipe fed.
 //
 // Design sources: "Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM" (v1 swizzled
 // TMA + descriptor, v3 warp specialisation with full/empty barriers, v4 2-CTA cluster
@@ -40,16 +44,20 @@ struct Bf16Params {
   unsigned debug_flags;
 };
 
-template <int CG, int STAGES>
+template <int CG, int STAGES, int ATOMS>
 struct Bf16Layout {
   static constexpr int BLOCK_M = 128;              // output rows per CTA = TMEM lanes
   static constexpr int BLOCK_N = 256;              // output columns per tile = MMA N
-  static constexpr int BLOCK_K = 64;               // BF16 elements per stage: one 128-byte swizzle row
+  static constexpr int ATOM_K = 64;                // BF16 elements of one 128-byte swizzle row
+  static constexpr int BLOCK_K = ATOM_K * ATOMS;   // K elements per stage
   static constexpr int UMMA_K = 16;                // K per tcgen05.mma kind::f16
+  static constexpr int KSTEPS = BLOCK_K / UMMA_K;  // MMAs per stage
   static constexpr int TILE_M = BLOCK_M * CG;      // output rows per tile (per CTA pair for CG = 2)
   static constexpr int B_ROWS = BLOCK_N / CG;      // rows of B each CTA loads per stage
-  static constexpr int A_BYTES = BLOCK_M * BLOCK_K * 2;
-  static constexpr int B_BYTES = B_ROWS * BLOCK_K * 2;
+  static constexpr int A_ATOM_BYTES = BLOCK_M * 128;  // one swizzle-row column of the A tile
+  static constexpr int B_ATOM_BYTES = B_ROWS * 128;
+  static constexpr int A_BYTES = A_ATOM_BYTES * ATOMS;
+  static constexpr int B_BYTES = B_ATOM_BYTES * ATOMS;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int ACC_COLS = BLOCK_N;         // FP32 accumulator columns per TMEM slot
   static constexpr int TMEM_COLS = 2 * ACC_COLS;   // two slots
@@ -75,12 +83,12 @@ struct Bf16Layout {
   static_assert(B_ROWS <= 256, "TMA box rows must not exceed 256");
 };
 
-template <int CG, int STAGES>
-__global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
+template <int CG, int STAGES, int ATOMS>
+__global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_c,
                      const Bf16Params p) {
-  using L = Bf16Layout<CG, STAGES>;
+  using L = Bf16Layout<CG, STAGES, ATOMS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // same offset in both CTAs of a pair
@@ -142,8 +150,11 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
         const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
                                                         : static_cast<int>(rank) * L::B_ROWS);
         const CUtensorMap* map_b = half ? &tmap_b_half : &tmap_b;
-        const uint32_t stage_bytes = L::A_BYTES + (half ? L::B_BYTES / 2 : L::B_BYTES);
+        const uint32_t atom_bytes = L::A_ATOM_BYTES + (half ? L::B_ATOM_BYTES / 2 : L::B_ATOM_BYTES);
         for (int kb = 0; kb < p.k_iters; ++kb) {
+          // swizzle-row columns of this stage that hold any of K (the last stage may hold fewer)
+          const int atoms = min(ATOMS, (p.K - kb * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K);
+          const uint32_t stage_bytes = atom_bytes * static_cast<uint32_t>(atoms);
           // First pass over the ring: parity 1 of a fresh barrier counts as complete.
           if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, wctx, status_code(kRoleProducer, stage))) {
             ok = false;
@@ -154,13 +165,19 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
           const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
           if constexpr (CG == 1) {
             mbar_arrive_expect_tx(full, stage_bytes);
-            tma_load_2d(sa, &tmap_a, kb * L::BLOCK_K, a_row, full);
-            tma_load_2d(sb, map_b, kb * L::BLOCK_K, b_row, full);
+            for (int a = 0; a < atoms; ++a) {
+              const int x = kb * L::BLOCK_K + a * L::ATOM_K;
+              tma_load_2d(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full);
+              tma_load_2d(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full);
+            }
           } else {
             const uint32_t full_leader = mapa_shared(full, 0);
             if (rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
-            tma_load_2d_pair(sa, &tmap_a, kb * L::BLOCK_K, a_row, full_leader);
-            tma_load_2d_pair(sb, map_b, kb * L::BLOCK_K, b_row, full_leader);
+            for (int a = 0; a < atoms; ++a) {
+              const int x = kb * L::BLOCK_K + a * L::ATOM_K;
+              tma_load_2d_pair(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full_leader);
+              tma_load_2d_pair(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full_leader);
+            }
           }
           if (++stage == STAGES) {
             stage = 0;
@@ -198,11 +215,17 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
+          // MMAs of the swizzle-row columns that hold any of K (all of them but in a ragged last stage)
+          const int ksteps = min(L::KSTEPS, (p.K - kb * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K * (L::ATOM_K / L::UMMA_K));
 #pragma unroll
-          for (int kk = 0; kk < L::BLOCK_K / L::UMMA_K; ++kk) {
-            const uint32_t koff = kk * L::UMMA_K * 2;  // bytes inside the 128-byte swizzle row
-            mma_f16<CG>(d_tmem, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc,
-                        (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < L::KSTEPS; ++kk) {
+            if (kk < ksteps) {
+              // column kk / 4 of the stage, then 32 bytes per MMA inside its 128-byte swizzle row
+              const uint32_t koff_a = (kk / 4) * L::A_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
+              const uint32_t koff_b = (kk / 4) * L::B_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
+              mma_f16<CG>(d_tmem, umma_desc_advance(a_desc, koff_a), umma_desc_advance(b_desc, koff_b), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           // Release the stage when these MMAs have read it; never wait here.
           if constexpr (CG == 1) mma_commit_local(bar_empty + 8 * stage);
@@ -308,10 +331,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES>::NUM_THREADS, 1)
 
 namespace {
 
-template <int CG, int STAGES>
+template <int CG, int STAGES, int ATOMS>
 struct Bf16Variant {
-  using L = Bf16Layout<CG, STAGES>;
-  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES>;
+  using L = Bf16Layout<CG, STAGES, ATOMS>;
+  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS>;
 
   // Co-resident clusters per device, queried once per device.
   static int max_active_clusters(int device) {
@@ -345,13 +368,13 @@ struct Bf16Variant {
   static int run(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                  const RunOptions& opt, int device, const DeviceInfo& info) {
     CUtensorMap ta, tb, tbh, tc;
-    int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, uint64_t(K) * 2, L::BLOCK_K,
+    int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, K, M, uint64_t(K) * 2, L::ATOM_K,
                             L::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == GEMM_OK)
-      st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::BLOCK_K, L::B_ROWS,
+      st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::ATOM_K, L::B_ROWS,
                           CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == GEMM_OK)  // B box of a half-width work item
-      st = encode_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::BLOCK_K,
+      st = encode_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::ATOM_K,
                           L::B_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st == GEMM_OK)
       st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
@@ -410,8 +433,9 @@ struct Bf16Variant {
   }
 };
 
-using Bf16OneCta = Bf16Variant<1, 4>;
-using Bf16Pair = Bf16Variant<2, 6>;
+using Bf16OneCta = Bf16Variant<1, 4, 1>;
+using Bf16Pair = Bf16Variant<2, 3, 2>;     // 3 stages of 128 K (64 KB per CTA): the default
+using Bf16PairK64 = Bf16Variant<2, 6, 1>;  // 6 stages of 64 K (32 KB per CTA)
 
 }  // namespace
 
@@ -426,6 +450,8 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
     case GEMM_KERNEL_DEFAULT:
     case GEMM_KERNEL_BF16_2CTA:
       return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
+    case GEMM_KERNEL_BF16_2CTA_K64:
+      return Bf16PairK64::run(A, B, C, M, N, K, stream, opt, device, *info);
     default:
       return GEMM_ERR_INVALID_ARG;
   }

@@ -7,13 +7,24 @@
 // tcgen05.cp moves them there from shared memory.
 //
 // Persistent CTA pairs (cta_group::2), a 256 x 256 output tile per pair, 256 K-elements
-// (128 bytes of codes per row, one 128-byte swizzle row) per pipeline stage:
-//   warp 0      TMA producer: per CTA and stage, A 16 KB, B 16 KB, SFA 2 KB, SFB 4 KB
-//   warp 1      MMA issuer (leader CTA) + TMEM allocator: 4 MMAs per stage
-//   warps 2..5  epilogue: all TMEM loads first, early release, then BF16 TMA stores
-//   warps 6, 7  scale copiers (leader CTA): 6 tcgen05.cp each per stage. One thread can
-//               issue a copy only about every 56 cycles, so the 12 copies of a stage would
-//               cost the MMA thread ~670 cycles per 512 cycles of MMAs.
+// (128 bytes of codes per row, one 128-byte swizzle row) per pipeline stage. Every
+// barrier wait, TMA issue, tcgen05.cp and tcgen05.mma costs its issuing thread tens to
+// hundreds of cycles (a wait about 160, a copy about 56, an MMA about 60), and a stage
+// keeps the tensor pipe busy only 512 cycles, so the per-stage work is spread over
+// threads of different warps, each well under that budget:
+//   warp 0      TMA producer of A (both CTAs); arms the leader's full barrier
+//   warp 1      TMA producer of B (both CTAs)
+//   warp 2      TMA producer of SFA (this CTA's 128 rows) and SFB (all 256 rows, one 3-D box)
+//   warp 3      MMA issuer (leader CTA) + TMEM allocator: one scale-ready wait per two
+//               stages, 4 MMAs and a commit per stage
+//   warps 4..11 epilogue: warp 4 + 4h + q reads TMEM lanes 32q.. of accumulator columns
+//               128h..128h+127 into registers (four loads, one wait), releases TMEM, then
+//               converts to BF16 and stores through shared memory with TMA
+//   warps 12..15 scale copiers (leader CTA): copier c copies the scales of MMA c of every
+//               stage (SFA, SFB rows 0-127, SFB rows 128-255) and commits to sf_ready
+// Warpgroups 0 and 3 give up registers (setmaxnreg) to the epilogue warpgroups 1 and 2,
+// which hold the whole 128 x 256 FP32 accumulator of a CTA in registers to free TMEM after
+// a single load latency (the one TMEM slot is the MMAs' only accumulator).
 // TMEM (512 columns): accumulator in columns 0..255 (one slot; the epilogue releases it as
 // soon as it has read it); a 5-deep scale ring after it, 48 columns per stage (16 for SFA:
 // 4 MMAs x 4 columns; 32 for SFB: 4 MMAs x 2 N-halves x 4 columns).
@@ -43,6 +54,7 @@ struct Nvfp4Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
+  int mma_group;  // stages the MMA issuer takes per scale-ready wait (1 .. STAGES)
 };
 
 template <int STAGES>
@@ -65,12 +77,16 @@ struct Nvfp4Layout {
   static constexpr int SF_COLS = KSTEPS * 4 + KSTEPS * 8;  // 16 + 32 TMEM columns per stage
   static constexpr int SF_TMEM_COL0 = ACC_COLS;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int EPI_WARPS = 4;
-  static constexpr int EPI_BUFS = 2;
-  static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;
-  static constexpr int COPY_WARP0 = 2 + EPI_WARPS;          // warps 6, 7
-  static constexpr int COPY_WARPS = 2;
+  // warp roles
+  static constexpr int WARP_PROD_A = 0, WARP_PROD_B = 1, WARP_PROD_SF = 2, WARP_MMA = 3;
+  // two epilogue warps per TMEM lane quadrant, one per 128-column half of the accumulator
+  static constexpr int EPI_WARP0 = 4, EPI_WARPS = 8;
+  static constexpr int COPY_WARP0 = 12, COPY_WARPS = KSTEPS;  // one copier per MMA of a stage
   static constexpr int NUM_THREADS = 32 * (COPY_WARP0 + COPY_WARPS);
+  // registers per thread after setmaxnreg (the launch gives 65536 / 512 -> 128)
+  static constexpr int REGS_LAUNCH = 128, REGS_LOW = 64, REGS_EPI = 184;
+  static constexpr int EPI_BUFS = 1;
+  static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -89,8 +105,273 @@ struct Nvfp4Layout {
   static_assert(SF_TMEM_COL0 + STAGES * SF_COLS <= TMEM_COLS, "scale ring does not fit in TMEM");
   static_assert(A_BYTES + B_BYTES == 32768, "A+B tile bytes per CTA per stage");
   static_assert(STAGE_BYTES == 38912, "38 KB stage of a CTA pair kernel");
-  static_assert(KSTEPS % COPY_WARPS == 0, "copiers split the MMAs of a stage evenly");
+  static_assert(NUM_THREADS == 512 && REGS_LAUNCH * NUM_THREADS <= 65536, "launch register budget");
+  static_assert(128 * (2 * REGS_LOW + 2 * REGS_EPI) <= REGS_LAUNCH * NUM_THREADS,
+                "setmaxnreg split exceeds the block's launch registers");
+  static_assert(EPI_WARP0 % 4 == 0 && EPI_WARPS == 8 && COPY_WARP0 % 4 == 0, "roles must fill whole warpgroups");
 };
+
+// Barrier addresses and per-CTA context shared by the roles.
+struct Nvfp4Ctx {
+  uint32_t base;       // 1024-aligned shared-memory base (same offset in both CTAs)
+  uint32_t warp, lane, rank;
+  int cluster_idx, num_clusters, my_items;
+  uint32_t tmem_base;
+  uint32_t bar_full, bar_empty, bar_sfready, bar_tfull, bar_tempty, bar_never, bar_drain;
+  WaitCtx wctx;
+};
+
+// ---------------------------------------------------------------- TMA producers (both CTAs)
+// warp 0: A (and the leader arms the full barrier with the bytes of both CTAs); warp 1: B;
+// warp 2: SFA and SFB. Each waits on its own CTA's empty barrier.
+template <int STAGES>
+__device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtensorMap* tmap_a,
+                                              const CUtensorMap* tmap_b, const CUtensorMap* tmap_b_half,
+                                              const CUtensorMap* tmap_sfa, const CUtensorMap* tmap_sfb,
+                                              const Nvfp4Ctx& x) {
+  using L = Nvfp4Layout<STAGES>;
+  if (x.lane != 0) return;
+  const int ksteps = p.K / L::UMMA_K;  // 512-byte scale blocks per 128 rows
+  uint32_t stage = 0, phase = 0;
+  bool ok = true;
+  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters) {
+    const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+    const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
+    const bool half = w.half >= 0;
+    const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(x.rank) * L::BLOCK_M;
+    const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(x.rank) * (L::B_ROWS / 2)
+                                                    : static_cast<int>(x.rank) * L::B_ROWS);
+    const CUtensorMap* map_b = half ? tmap_b_half : tmap_b;
+    // a half item loads half the B rows; the scales of the whole tile are loaded either way
+    const uint32_t stage_bytes = L::STAGE_BYTES - (half ? L::B_BYTES / 2 : 0);
+    const int sfa_block = (a_row / 128) * ksteps;
+    for (int kb = 0; kb < p.k_iters; ++kb) {
+      // First pass over the ring: parity 1 of a fresh barrier counts as complete.
+      if (!wait_phase_inline(x.bar_empty + 8 * stage, phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | stage))) {
+        ok = false;
+        break;
+      }
+      const uint32_t full = x.bar_full + 8 * stage;
+      const uint32_t full_leader = mapa_shared(full, 0);
+      const int kx = kb * (L::BLOCK_K / 2);
+      const int ky = kb * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
+      if (x.warp == L::WARP_PROD_A) {
+        // one arrival with the bytes of both CTAs; the other loads may land before it
+        if (x.rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
+        tma_load_2d_pair(x.base + L::OFF_A + stage * L::A_BYTES, tmap_a, kx, a_row, full_leader);
+      } else if (x.warp == L::WARP_PROD_B) {
+        tma_load_2d_pair(x.base + L::OFF_B + stage * L::B_BYTES, map_b, kx, b_row, full_leader);
+      } else {
+        tma_load_2d_pair(x.base + L::OFF_SFA + stage * L::SFA_BYTES, tmap_sfa, 0, sfa_block + ky, full_leader);
+        // both 128-row blocks of the tile's SFB (row blocks 2n and 2n+1), steps ky .. ky+3
+        tma_load_3d_pair(x.base + L::OFF_SFB + stage * L::SFB_BYTES, tmap_sfb, 0, ky, tc.n_blk * 2, full_leader);
+      }
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!ok) settle_after_abort();
+}
+
+// ---------------------------------------------------------------- scale copiers (leader)
+// Copier c moves, for every stage, the scale blocks of MMA c (SFA, SFB rows 0-127, SFB
+// rows 128-255: 3 copies) from shared memory to the stage's TMEM scale slot, then commits
+// to sf_ready. Waiting for the stage's data also guarantees that the MMAs STAGES stages
+// earlier, which read the same TMEM slot, have completed: the producers could not reload
+// the stage before their commit.
+template <int STAGES>
+__device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx& x) {
+  using L = Nvfp4Layout<STAGES>;
+  if (x.rank != 0 || x.lane != 0) return;
+  const uint32_t c = x.warp - L::COPY_WARP0;
+  const long long total = static_cast<long long>(x.my_items > 0 ? x.my_items : 0) * p.k_iters;
+  const uint64_t sfa0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFA, 128), c * L::SF_BLOCK);
+  const uint64_t sfb0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFB, 128), c * L::SF_BLOCK);
+  uint64_t sfa = sfa0, sfb = sfb0;
+  const uint32_t col0 = x.tmem_base + L::SF_TMEM_COL0;
+  uint32_t col = col0;
+  uint32_t stage = 0, phase = 0;
+  bool ok = true;
+  for (long long g = 0; g < total; ++g) {
+    if (!wait_phase_inline(x.bar_full + 8 * stage, phase, x.wctx, status_code(kRoleScales, 0x300 + stage))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    tmem_cp_32x128b_warpx4<2>(col + 4 * c, sfa);
+    tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * c, sfb);
+    tmem_cp_32x128b_warpx4<2>(col + 20 + 8 * c, umma_desc_advance(sfb, L::SFB_BYTES / 2));
+    mma_commit_pair_multicast(x.bar_sfready + 8 * stage, 0x1);
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1u;
+      sfa = sfa0;
+      sfb = sfb0;
+      col = col0;
+    } else {
+      sfa = umma_desc_advance(sfa, L::SFA_BYTES);
+      sfb = umma_desc_advance(sfb, L::SFB_BYTES);
+      col += L::SF_COLS;
+    }
+  }
+  if (!ok) settle_after_abort();
+}
+
+// ---------------------------------------------------------------- MMA issuer (leader)
+template <int STAGES>
+__device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x) {
+  using L = Nvfp4Layout<STAGES>;
+  if (x.rank != 0 || x.lane != 0) return;
+  constexpr uint32_t IDESC_FULL = idesc_nvf4(L::TILE_M, L::BLOCK_N);
+  constexpr uint32_t IDESC_HALF = idesc_nvf4(L::TILE_M, L::BLOCK_N / 2);
+  uint32_t stage = 0, phase = 0;
+  bool ok = true;
+  if (p.debug_flags & 1u) ok = wait_phase_inline(x.bar_never, 0, x.wctx, status_code(kRoleMma, 0xFFFF));
+  // Per-stage operand descriptors and scale columns, advanced with the ring position.
+  const uint64_t a_desc0 = umma_desc_sw128(x.base + L::OFF_A), b_desc0 = umma_desc_sw128(x.base + L::OFF_B);
+  const uint32_t sf_col0 = x.tmem_base + L::SF_TMEM_COL0;
+  uint64_t a_desc = a_desc0, b_desc = b_desc0;
+  uint32_t sf_col = sf_col0;
+  int it = 0;
+  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
+    const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+    const uint32_t idesc = w.half >= 0 ? IDESC_HALF : IDESC_FULL;
+    const uint32_t sfb_half_col = w.half > 0 ? 4u : 0u;  // scale columns of the item's N-half
+    if (!wait_phase_inline(x.bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u, x.wctx, status_code(kRoleMma, 0x100))) {
+      ok = false;
+      break;
+    }
+    tc_fence_after_sync();
+    for (int kb = 0; kb < p.k_iters;) {
+      // Several stages per wait where the tile has them. Each copier commits its stages in
+      // order, and a commit covers all earlier copies of its thread, so the scale-ready
+      // phase of a later stage implies the earlier ones'; the copiers copied each stage
+      // only after its full barrier, so the stages' tiles are in shared memory too.
+      const int n = min(p.mma_group, p.k_iters - kb);
+      uint32_t last = stage, last_phase = phase;
+      for (int u = 1; u < n; ++u)
+        if (++last == STAGES) {
+          last = 0;
+          last_phase ^= 1u;
+        }
+      if (!wait_phase_inline(x.bar_sfready + 8 * last, last_phase, x.wctx, status_code(kRoleMma, 0x200 + last))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      for (int u = 0; u < n; ++u, ++kb) {
+#pragma unroll
+        for (int j = 0; j < L::KSTEPS; ++j) {
+          const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
+          mma_nvf4<2>(x.tmem_base, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc,
+                      sf_col + 4 * j, sf_col + 16 + 8 * j + sfb_half_col, (kb | j) != 0 ? 1u : 0u);
+        }
+        // release the stage when these MMAs have read it (shared memory and TMEM scales)
+        mma_commit_pair_multicast(x.bar_empty + 8 * stage, 0x3);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+          a_desc = a_desc0;
+          b_desc = b_desc0;
+          sf_col = sf_col0;
+        } else {
+          a_desc = umma_desc_advance(a_desc, L::A_BYTES);
+          b_desc = umma_desc_advance(b_desc, L::B_BYTES);
+          sf_col += L::SF_COLS;
+        }
+      }
+    }
+    if (!ok) break;
+    mma_commit_pair_multicast(x.bar_tfull, 0x3);
+  }
+  if (!ok) {
+    mma_commit_pair_multicast(x.bar_drain, 0x1);
+    const uint64_t t0 = globaltimer_ns();  // bounded: the issued MMAs finish or the limit passes
+    while (!mbar_try_wait_suspend(x.bar_drain, 0, 20000u) && globaltimer_ns() - t0 < x.wctx.limit_ns) {
+    }
+    settle_after_abort();
+  }
+}
+
+// ---------------------------------------------------------------- epilogue (warps 4..11)
+template <int STAGES>
+__device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtensorMap* tmap_c, const Nvfp4Ctx& x) {
+  using L = Nvfp4Layout<STAGES>;
+  const uint32_t lane = x.lane;
+  const uint32_t q = x.warp & 3u;                  // this warp may access TMEM lanes 32q .. 32q+31
+  const uint32_t epi = x.warp - L::EPI_WARP0;
+  const int h = static_cast<int>(epi >> 2);        // accumulator columns 128h .. 128h+127
+  const uint32_t buf = x.base + L::OFF_EPI + epi * L::EPI_BUF_BYTES;
+  const uint32_t tempty_leader = mapa_shared(x.bar_tempty, 0);
+  int it = 0;
+  for (int i = x.cluster_idx; i < p.num_items; i += x.num_clusters, ++it) {
+    const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+    const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
+    const int width = w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N;  // accumulator columns of the item
+    if (__all_sync(0xffffffffu, wait_phase_inline(x.bar_tfull, static_cast<uint32_t>(it) & 1u, x.wctx,
+                                                   status_code(kRoleEpilogue, 0))) == 0)
+      break;
+    tc_fence_after_sync();
+    const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(x.rank) * L::BLOCK_M + static_cast<int>(q) * 32;
+    const int col0 = tc.n_blk * L::BLOCK_N + (w.half > 0 ? L::BLOCK_N / 2 : 0) + h * 128;
+    const uint32_t taddr = x.tmem_base + ((q * 32u) << 16) + static_cast<uint32_t>(h) * 128u;
+    const bool live = row0 < p.M && h * 128 < width;
+    uint32_t v[4][32];
+    if (live) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+      tmem_ld_wait();
+    }
+    // this warp's part of the accumulator is in registers: release TMEM, then convert and store
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cluster(tempty_leader);
+    if (live) {
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = col0 + cc * 64;
+        if (col < p.N) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            pk[e] = pack_bf16x2_rn(v[2 * cc][2 * e], v[2 * cc][2 * e + 1]);
+            pk[16 + e] = pack_bf16x2_rn(v[2 * cc + 1][2 * e], v[2 * cc + 1][2 * e + 1]);
+          }
+          if (lane == 0) bulk_wait_group_read<0>();  // the store that last read `buf` is done
+          __syncwarp();
+          // row `lane` of the 32 x 64 staging tile, 16-byte chunk j at j ^ (row % 8):
+          // the C tensor map's 128-byte swizzle, bank-conflict free
+          const uint32_t row_addr = buf + lane * 128u;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
+                         pk[4 * j + 2], pk[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(tmap_c, buf, col, row0);
+            bulk_commit_group();
+          }
+        }
+      }
+    }
+  }
+  if (lane == 0) bulk_wait_group<0>();
+  __syncwarp();
+}
+
+// All roles meet here once their work is done; the MMA warp (which allocated TMEM) frees it.
+template <int STAGES>
+__device__ __forceinline__ void teardown(const Nvfp4Ctx& x) {
+  tc_fence_before_sync();
+  cluster_sync_all();
+  if (x.warp == Nvfp4Layout<STAGES>::WARP_MMA) {
+    tc_fence_after_sync();
+    tmem_dealloc<2>(x.tmem_base, Nvfp4Layout<STAGES>::TMEM_COLS);
+  }
+}
 
 template <int STAGES>
 __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
@@ -101,37 +382,36 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   using L = Nvfp4Layout<STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // same offset in both CTAs of a pair
-  uint8_t* smem = smem_raw + (base - raw);
-
-  const uint32_t warp = threadIdx.x >> 5;
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const int cluster_idx = static_cast<int>(blockIdx.x) / L::CG;
-  const int num_clusters = static_cast<int>(gridDim.x) / L::CG;
-  const int my_items = (p.num_items - cluster_idx + num_clusters - 1) / num_clusters;
-
-  const uint32_t bar_full = base + L::OFF_BAR;          // stage landed (leader's, bytes of both CTAs)
-  const uint32_t bar_empty = bar_full + 8 * STAGES;     // stage consumed by the MMAs (both CTAs)
-  const uint32_t bar_sfready = bar_empty + 8 * STAGES;  // stage's scales copied to TMEM (leader's)
-  const uint32_t bar_tfull = bar_sfready + 8 * STAGES;  // accumulator ready
-  const uint32_t bar_tempty = bar_tfull + 8;            // accumulator drained (leader's, 8 arrivals)
-  const uint32_t bar_never = bar_tempty + 8;            // nobody arrives (timeout-path test)
-  const uint32_t bar_drain = bar_never + 8;             // MMA drain after an abort
+  Nvfp4Ctx x;
+  x.base = (raw + 1023u) & ~1023u;  // same offset in both CTAs of a pair
+  uint8_t* smem = smem_raw + (x.base - raw);
+  x.warp = threadIdx.x >> 5;
+  x.lane = threadIdx.x & 31;
+  x.rank = cluster_ctarank();
+  x.cluster_idx = static_cast<int>(blockIdx.x) / L::CG;
+  x.num_clusters = static_cast<int>(gridDim.x) / L::CG;
+  x.my_items = (p.num_items - x.cluster_idx + x.num_clusters - 1) / x.num_clusters;
+  x.bar_full = x.base + L::OFF_BAR;             // stage landed (leader's, bytes of both CTAs)
+  x.bar_empty = x.bar_full + 8 * STAGES;        // stage consumed by the MMAs (both CTAs)
+  x.bar_sfready = x.bar_empty + 8 * STAGES;     // stage's scales copied to TMEM (leader's)
+  x.bar_tfull = x.bar_sfready + 8 * STAGES;     // accumulator ready
+  x.bar_tempty = x.bar_tfull + 8;               // accumulator drained (leader's, 8 arrivals)
+  x.bar_never = x.bar_tempty + 8;               // nobody arrives (timeout-path test)
+  x.bar_drain = x.bar_never + 8;                // MMA drain after an abort
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
-  const WaitCtx wctx{abort_flag, p.status, p.wait_limit_ns};
+  x.wctx = WaitCtx{abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0 && lane == 0) {
+  if (x.warp == 0 && x.lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
-      mbar_init(bar_empty + 8 * s, 1);
-      mbar_init(bar_sfready + 8 * s, L::COPY_WARPS);
+      mbar_init(x.bar_full + 8 * s, 1);
+      mbar_init(x.bar_empty + 8 * s, 1);
+      mbar_init(x.bar_sfready + 8 * s, L::COPY_WARPS);
     }
-    mbar_init(bar_tfull, 1);
-    mbar_init(bar_tempty, L::EPI_WARPS * L::CG);
-    mbar_init(bar_never, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(x.bar_tfull, 1);
+    mbar_init(x.bar_tempty, L::EPI_WARPS * L::CG);
+    mbar_init(x.bar_never, 1);
+    mbar_init(x.bar_drain, 1);
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
     prefetch_tensormap(&tmap_a);
@@ -141,242 +421,33 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     prefetch_tensormap(&tmap_sfb);
     prefetch_tensormap(&tmap_c);
   }
-  if (warp == 1) {
+  if (x.warp == L::WARP_MMA) {
     tmem_alloc<2>(smem_u32(tmem_slot), L::TMEM_COLS);
     tmem_relinquish<2>();
   }
   tc_fence_before_sync();
   cluster_sync_all();
   tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_slot;
+  x.tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer (both CTAs)
-    if (lane == 0) {
-      const int ksteps = p.K / L::UMMA_K;  // 512-byte scale blocks per 128 rows
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters) {
-        const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
-        const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
-        const bool half = w.half >= 0;
-        const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
-        const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
-                                                        : static_cast<int>(rank) * L::B_ROWS);
-        const CUtensorMap* map_b = half ? &tmap_b_half : &tmap_b;
-        // a half item loads half the B rows; the scales of the whole tile are loaded either way
-        const uint32_t stage_bytes = L::STAGE_BYTES - (half ? L::B_BYTES / 2 : 0);
-        const int sfa_block = (a_row / 128) * ksteps;
-        const int sfb_block = (tc.n_blk * 2) * ksteps;
-        for (int kb = 0; kb < p.k_iters; ++kb) {
-          // First pass over the ring: parity 1 of a fresh barrier counts as complete.
-          if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, wctx, status_code(kRoleProducer, stage))) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = bar_full + 8 * stage;
-          if (rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
-          const uint32_t full_leader = mapa_shared(full, 0);
-          const int x = kb * (L::BLOCK_K / 2);
-          const int y = kb * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
-          tma_load_2d_pair(base + L::OFF_A + stage * L::A_BYTES, &tmap_a, x, a_row, full_leader);
-          tma_load_2d_pair(base + L::OFF_B + stage * L::B_BYTES, map_b, x, b_row, full_leader);
-          tma_load_2d_pair(base + L::OFF_SFA + stage * L::SFA_BYTES, &tmap_sfa, 0, sfa_block + y, full_leader);
-          tma_load_2d_pair(base + L::OFF_SFB + stage * L::SFB_BYTES, &tmap_sfb, 0, sfb_block + y, full_leader);
-          tma_load_2d_pair(base + L::OFF_SFB + stage * L::SFB_BYTES + L::SFB_BYTES / 2, &tmap_sfb, 0,
-                           sfb_block + ksteps + y, full_leader);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) settle_after_abort();
-    }
+  // One branch per warpgroup, each with one register-limit change for all its warps: the
+  // epilogue warpgroup takes the registers that warpgroups 0 and 2 give up. Each branch
+  // runs to the end of the kernel (the code after a change of limit belongs to one limit).
+  if (x.warp < L::EPI_WARP0) {
+    regs_decrease<L::REGS_LOW>();
+    if (x.warp <= L::WARP_PROD_SF) producer_role<STAGES>(p, &tmap_a, &tmap_b, &tmap_b_half, &tmap_sfa, &tmap_sfb, x);
+    else mma_role<STAGES>(p, x);
     __syncwarp();
-  } else if (warp >= L::COPY_WARP0) {
-    // ------------------------------------------------------------ scale copiers (leader)
-    // Copier c moves, for every stage, the scale blocks of MMAs 2c and 2c+1 (SFA, SFB rows
-    // 0-127, SFB rows 128-255: 6 copies) from shared memory to the stage's TMEM scale slot,
-    // then commits to sf_ready. Waiting for the stage's data also guarantees that the MMAs
-    // STAGES stages earlier, which read the same TMEM slot, have completed: the producer
-    // could not reload the stage before their commit.
-    const int c = static_cast<int>(warp) - L::COPY_WARP0;
-    if (rank == 0 && lane == 0) {
-      const long long total = static_cast<long long>(my_items > 0 ? my_items : 0) * p.k_iters;
-      const uint64_t sfa0 = umma_desc_plain(base + L::OFF_SFA, 128), sfb0 = umma_desc_plain(base + L::OFF_SFB, 128);
-      uint64_t sfa = sfa0, sfb = sfb0;
-      uint32_t col = tmem_base + L::SF_TMEM_COL0;
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (long long g = 0; g < total; ++g) {
-        if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleScales, 0x300 + stage))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int jj = 0; jj < L::KSTEPS / L::COPY_WARPS; ++jj) {
-          const uint32_t j = c * (L::KSTEPS / L::COPY_WARPS) + jj;
-          tmem_cp_32x128b_warpx4<2>(col + 4 * j, umma_desc_advance(sfa, j * L::SF_BLOCK));
-          tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * j, umma_desc_advance(sfb, j * L::SF_BLOCK));
-          tmem_cp_32x128b_warpx4<2>(col + 20 + 8 * j, umma_desc_advance(sfb, L::SFB_BYTES / 2 + j * L::SF_BLOCK));
-        }
-        mma_commit_pair_multicast(bar_sfready + 8 * stage, 0x1);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-          sfa = sfa0;
-          sfb = sfb0;
-          col = tmem_base + L::SF_TMEM_COL0;
-        } else {
-          sfa = umma_desc_advance(sfa, L::SFA_BYTES);
-          sfb = umma_desc_advance(sfb, L::SFB_BYTES);
-          col += L::SF_COLS;
-        }
-      }
-      if (!ok) settle_after_abort();
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (leader)
-    if (rank == 0 && lane == 0) {
-      constexpr uint32_t IDESC_FULL = idesc_nvf4(L::TILE_M, L::BLOCK_N);
-      constexpr uint32_t IDESC_HALF = idesc_nvf4(L::TILE_M, L::BLOCK_N / 2);
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
-      // Per-stage operand descriptors and scale columns, advanced with the ring position.
-      const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
-      const uint32_t sf_col0 = tmem_base + L::SF_TMEM_COL0;
-      uint64_t a_desc = a_desc0, b_desc = b_desc0;
-      uint32_t sf_col = sf_col0;
-      int it = 0;
-      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
-        const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
-        const uint32_t idesc = w.half >= 0 ? IDESC_HALF : IDESC_FULL;
-        const uint32_t sfb_half_col = w.half > 0 ? 4u : 0u;  // scale columns of the item's N-half
-        if (!wait_phase(bar_tempty, (static_cast<uint32_t>(it) & 1u) ^ 1u, wctx, status_code(kRoleMma, 0x100))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        for (int kb = 0; kb < p.k_iters; ++kb) {
-          // The stage's scales are in TMEM. The copiers copied them only after the stage's
-          // full barrier completed, so its tiles are in shared memory too.
-          if (!wait_phase(bar_sfready + 8 * stage, phase, wctx, status_code(kRoleMma, 0x200 + stage))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-#pragma unroll
-          for (int j = 0; j < L::KSTEPS; ++j) {
-            const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
-            mma_nvf4<2>(tmem_base, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc,
-                        sf_col + 4 * j, sf_col + 16 + 8 * j + sfb_half_col, (kb | j) != 0 ? 1u : 0u);
-          }
-          // release the stage when these MMAs have read it (shared memory and TMEM scales)
-          mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-            a_desc = a_desc0;
-            b_desc = b_desc0;
-            sf_col = sf_col0;
-          } else {
-            a_desc = umma_desc_advance(a_desc, L::A_BYTES);
-            b_desc = umma_desc_advance(b_desc, L::B_BYTES);
-            sf_col += L::SF_COLS;
-          }
-        }
-        if (!ok) break;
-        mma_commit_pair_multicast(bar_tfull, 0x3);
-      }
-      if (!ok) {
-        mma_commit_pair_multicast(bar_drain, 0x1);
-        wait_phase_slow(bar_drain, 0, wctx, status_code(kRoleMma, 0xFFFE), false);
-        settle_after_abort();
-      }
-    }
-    __syncwarp();
+    teardown<STAGES>(x);
+  } else if (x.warp < L::COPY_WARP0) {
+    regs_increase<L::REGS_EPI>();
+    epilogue_role<STAGES>(p, &tmap_c, x);
+    teardown<STAGES>(x);
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const uint32_t q = warp & 3u;  // this warp may access TMEM lanes 32q .. 32q+31
-    const uint32_t epi = warp - 2u;
-    const uint32_t stage_base = base + L::OFF_EPI + epi * L::EPI_BUFS * L::EPI_BUF_BYTES;
-    const uint32_t tempty_leader = mapa_shared(bar_tempty, 0);
-    uint32_t ebuf = 0;
-    int it = 0;
-    for (int i = cluster_idx; i < p.num_items; i += num_clusters, ++it) {
-      const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
-      const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
-      const int chunks = w.half >= 0 ? 2 : 4;  // 64-column chunks of the item
-      if (!wait_phase_warp(bar_tfull, static_cast<uint32_t>(it) & 1u, wctx, status_code(kRoleEpilogue, 0))) break;
-      tc_fence_after_sync();
-      const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M + static_cast<int>(q) * 32;
-      const int col0 = tc.n_blk * L::BLOCK_N + (w.half > 0 ? L::BLOCK_N / 2 : 0);
-      const uint32_t taddr = tmem_base + ((q * 32u) << 16);
-      const bool rows_live = row0 < p.M;
-      uint32_t pk[4][32];
-      if (rows_live) {
-        // two rounds of 128 columns (four loads, one wait each): the accumulator drains
-        // after two load latencies instead of four
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          if (r * 2 < chunks) {
-            uint32_t v[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + r * 128 + c * 32, v[c]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                pk[2 * r + c2][e] = pack_bf16x2_rn(v[2 * c2][2 * e], v[2 * c2][2 * e + 1]);
-                pk[2 * r + c2][16 + e] = pack_bf16x2_rn(v[2 * c2 + 1][2 * e], v[2 * c2 + 1][2 * e + 1]);
-              }
-          }
-        }
-      }
-      // the accumulator is in registers: release TMEM before converting / storing
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader);
-      if (rows_live) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int col = col0 + c * 64;
-          if (c < chunks && col < p.N) {
-            const uint32_t buf = stage_base + ebuf * L::EPI_BUF_BYTES;
-            if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
-            __syncwarp();
-            // row `lane` of the 32 x 64 staging tile, 16-byte chunk j at j ^ (row % 8):
-            // the C tensor map's 128-byte swizzle, bank-conflict free
-            const uint32_t row_addr = buf + lane * 128u;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[c][4 * j],
-                           pk[c][4 * j + 1], pk[c][4 * j + 2], pk[c][4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&tmap_c, buf, col, row0);
-              bulk_commit_group();
-            }
-            ebuf ^= 1u;
-          }
-        }
-      }
-    }
-    if (lane == 0) bulk_wait_group<0>();
+    regs_decrease<L::REGS_LOW>();
+    copier_role<STAGES>(p, x);
     __syncwarp();
-  }
-
-  tc_fence_before_sync();
-  cluster_sync_all();
-  if (warp == 1) {
-    tc_fence_after_sync();
-    tmem_dealloc<2>(tmem_base, L::TMEM_COLS);
+    teardown<STAGES>(x);
   }
 }
 
@@ -441,9 +512,14 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   if (st == GEMM_OK)
     st = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFA, 128, uint64_t(ceil_div(M, 128)) * ksteps, 512,
                         128, NL::KSTEPS, CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, 128, uint64_t(ceil_div(N, 128)) * ksteps, 512,
-                        128, NL::KSTEPS, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (st == GEMM_OK) {
+    // SFB as [row block][64-K step][128 words]: one box holds a stage's 4 steps of both
+    // row blocks of a 256-row tile, in the order the copiers read them
+    const uint64_t dims[3] = {128, ksteps, uint64_t(ceil_div(N, 128))};
+    const uint64_t strides[2] = {512, ksteps * 512};
+    const uint32_t box[3] = {128, NL::KSTEPS, 2};
+    st = encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, dims, strides, box);
+  }
   if (st == GEMM_OK)
     st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
                         CU_TENSOR_MAP_SWIZZLE_128B);
@@ -462,6 +538,7 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.status = device_status_word(device);
   p.wait_limit_ns = opt.wait_limit_ns;
   p.debug_flags = opt.debug_flags;
+  p.mma_group = 2;  // measured: 1 -> 15% slower, 3 -> 4% slower (the wait for the third stage)
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = max_active_clusters(device);

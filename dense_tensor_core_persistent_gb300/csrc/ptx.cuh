@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D tile load for a CTA pair (see tma_load_2d_pair); coordinates innermost first.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(m), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
 // 2-D tile store shared -> global, tracked by the calling thread's bulk async-groups.
 // Elements outside the tensor's extent are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, uint32_t src, int32_t x, int32_t y) {
@@ -192,6 +202,19 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 }
 __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- register reallocation
+
+// Per-warpgroup register limits: every warp of a warpgroup executes the same call. The
+// decreases must free at least what the increases take from the block's launch total.
+template <uint32_t REGS>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS) : "memory");
+}
+template <uint32_t REGS>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05: MMA
@@ -283,6 +306,14 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo_bits, uint32_t hi_bits) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
+  return d;
+}
+
+// Same conversion, kept in program order with the other volatile asm (TMEM loads): lets
+// a caller bound how many loaded-but-unconverted registers are live at once.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn_ordered(uint32_t lo_bits, uint32_t hi_bits) {
+  uint32_t d;
+  asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
   return d;
 }
 

@@ -186,7 +186,9 @@ int gemm_get_device_status(void* stream, uint32_t* detail);
 typedef enum {
     GEMM_KERNEL_DEFAULT = 0,        /* what gemm_bf16 / gemm_nvfp4 launch */
     GEMM_KERNEL_BF16_1CTA = 1,      /* BF16, cta_group::1, 128 x 256 tile per CTA */
-    GEMM_KERNEL_BF16_2CTA = 2       /* BF16, cta_group::2, 256 x 256 tile per CTA pair */
+    GEMM_KERNEL_BF16_2CTA = 2,      /* BF16, cta_group::2, 256 x 256 tile per CTA pair, 3 stages of
+                                       128 K (8 MMAs per stage): the default */
+    GEMM_KERNEL_BF16_2CTA_K64 = 3   /* the same with 6 stages of 64 K (4 MMAs per stage) */
 } gemm_kernel_t;
 
 typedef struct {

@@ -32,6 +32,8 @@ VARIANTS = {
     "pair_tile_per_cluster": dict(persistent=0),
     "single_cta": dict(kernel=g.GEMM_KERNEL_BF16_1CTA, persistent=0),
     "single_cta_persistent": dict(kernel=g.GEMM_KERNEL_BF16_1CTA),
+    "pair_k64_persistent": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_K64),
+    "pair_k64_tile_per_cluster": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_K64, persistent=0),
 }
 
 
@@ -76,7 +78,7 @@ def test_ragged_shapes(variant, shape):
 
 
 @pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 1), (3, 2), (5, 3), (7, 16)])
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
 def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
     """Few clusters, many tiles each: the stage ring and the two TMEM slots cycle across tiles."""
     M, N, K = 1280, 1024, 456   # 5 x 4 tiles of 256 x 256, 8 K stages (last one partial)
@@ -86,7 +88,7 @@ def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
 
 
 @pytest.mark.parametrize("max_clusters", [16, 9, 19])
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
 def test_tail_wave_split_into_halves(kernel, max_clusters):
     """A last wave at most half full is computed as N-halves of its tiles (N = 128 MMAs)."""
     M, N, K = 1280, 1000, 328     # 5 x 4 tiles (2-CTA) with a ragged last column block
@@ -205,7 +207,7 @@ def test_one_launch_per_call():
     assert g.launch_count() == before + 1
 
 
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel):
     """debug flag 1: the MMA issuer waits on a barrier nothing arrives on. The bounded wait
     expires (100 ms), the kernel records GEMM_ERR_TIMEOUT and exits; the context stays usable."""
