@@ -337,7 +337,8 @@ def run_ours(args, cfg, world, rank, local):
     outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     stream = torch.cuda.Stream(device=dev)
     opts = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
-                     persistent=0 if args.no_persistent else 1, no_tail_split=1 if args.no_tail_split else 0)
+                     persistent=0 if args.no_persistent else 1, no_tail_split=1 if args.no_tail_split else 0,
+                     no_pdl=1 if args.no_pdl else 0)
     flops = 2.0 * M * N * K
     torch.cuda.synchronize()
 
@@ -425,6 +426,18 @@ def run_ours(args, cfg, world, rank, local):
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * NOMINAL_FP4_OVER_BF16
         peak_note = f"{peak_src} BF16 burst x nominal FP4/BF16 ratio 6"
     achieved = flops / per_launch_s / 1e12
+    # The MMA instruction's own rate on this GPU (FLOP per SM clock), and what it gives at the
+    # SM clock sampled during the timed region: the ceiling for a kernel built from it.
+    rate = None
+    try:
+        fpc = g.measure_mma_rate(g.GEMM_MMA_BF16 if cfg["kind"] == "bf16" else g.GEMM_MMA_NVFP4)
+        mhz = clock_info.get("sm_mhz") if clock_info else None
+        rate = {"flop_per_clk_per_sm": fpc, "sms": props.multi_processor_count}
+        if mhz:
+            ceiling = fpc * props.multi_processor_count * mhz * 1e6 / 1e12
+            rate.update({"ceiling_at_sampled_clock": ceiling, "frac_of_ceiling": achieved / ceiling})
+    except Exception as e:  # report, do not fail the benchmark line
+        rate = {"error": str(e)}
     traffic = recorded_traffic(cfg["workload"] + ("" if cfg["kind"] == "bf16" else f"_{args.scales}"), cfg["kind"])
     cpu = cpu_baseline(cfg, args.cpu_seconds) if not args.no_cpu_baseline else None
     if cpu:
@@ -450,10 +463,11 @@ def run_ours(args, cfg, world, rank, local):
             "kernel": {0: "default (2-CTA persistent, 128-K stages)", 1: "1-CTA", 2: "2-CTA, 128-K stages",
                        3: "2-CTA, 64-K stages"}[args.kernel]
             + ("" if not args.no_persistent else ", one tile per cluster")
-            + (", no tail split" if args.no_tail_split else ""),
+            + (", no tail split" if args.no_tail_split else "")
+            + (", plain launches (no programmatic dependent launch)" if args.no_pdl else ""),
             "scales": (None if cfg["kind"] == "bf16" else
                        "blocked tensor-core layout (packed once at input setup)" if args.scales == "blocked"
-                       else "row-major [rows][K/16], rearranged inside the kernel"),
+                       else "row-major [rows][K/16], packed to the tensor-core layout inside each call"),
             "group_m": args.group_m or "auto",
             "baseline": "HGEMM v7 on GB300, 1980.925 TFLOP/s (page 1 Performance table)" if baseline else None,
         },
@@ -466,6 +480,7 @@ def run_ours(args, cfg, world, rank, local):
             "traffic": traffic,
             "peak_source": peak_note,
             "algorithmic_flops_per_launch": flops,
+            "instruction_rate": rate,
         },
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -484,6 +499,7 @@ def main():
     ap.add_argument("--config", default="c3", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernel", type=int, default=0)
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic stream serialization")
     ap.add_argument("--group-m", type=int, default=0)
     ap.add_argument("--max-clusters", type=int, default=0)
     ap.add_argument("--no-persistent", action="store_true")

@@ -40,7 +40,7 @@ EXPORTS = (
     "gemm_bf16", "gemm_nvfp4", "gemm_status_string", "gemm_get_device_status", "gemm_bf16_ex",
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
-    "gemm_nvfp4_noalloc",
+    "gemm_nvfp4_noalloc", "gemm_measure_mma_rate",
 )
 
 
@@ -59,13 +59,14 @@ class gemm_options_t(ctypes.Structure):
         ("wait_limit_us", ctypes.c_uint32),
         ("debug_flags", ctypes.c_uint32),
         ("no_tail_split", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("no_pdl", ctypes.c_int),
+        ("reserved", ctypes.c_int * 2),
     ]
 
 
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0):
-    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split)
+            no_tail_split=0, no_pdl=0):
+    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl)
 
 
 _lib = None
@@ -109,6 +110,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_nvfp4_noalloc.restype = I
         l.gemm_launch_count.argtypes = []
         l.gemm_launch_count.restype = ctypes.c_ulonglong
+        l.gemm_measure_mma_rate.argtypes = [I, ctypes.POINTER(ctypes.c_double)]
+        l.gemm_measure_mma_rate.restype = I
         _lib = l
     return _lib
 
@@ -220,6 +223,17 @@ def choose_group_m(M, N, K, tile_m, tile_n, elem_bytes_x2, concurrent_tiles, l2_
 
 def launch_count() -> int:
     return lib().gemm_launch_count()
+
+
+GEMM_MMA_BF16 = 0
+GEMM_MMA_NVFP4 = 1
+
+
+def measure_mma_rate(kind: int) -> float:
+    """FLOP per SM clock of back-to-back M=256 N=256 MMAs of `kind` on the current device."""
+    out = ctypes.c_double(0.0)
+    _check(lib().gemm_measure_mma_rate(kind, ctypes.byref(out)), "gemm_measure_mma_rate")
+    return out.value
 
 
 # ---------------------------------------------------------------- torch-tensor conveniences

@@ -169,9 +169,10 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o == nullptr) return GEMM_OK;
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 2; ++i)
     if (o->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
+  if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
@@ -181,6 +182,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->group_m = o->group_m;
   r->max_clusters = o->max_clusters;
   r->tail_split = o->no_tail_split ? 0 : 1;
+  r->pdl = o->no_pdl ? 0 : 1;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -280,7 +282,7 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   }
   uint8_t* sfa_blk = static_cast<uint8_t*>(ws);
   uint8_t* sfb_blk = sfa_blk + bytes_a;
-  st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s);
+  st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s, opt.pdl);
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, sfa_blk, B, sfb_blk, C, M, N, K, s, opt);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;

@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
   if constexpr (CG == 2) cluster_sync_all(); else __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up is done: the next kernel may start its own. Every global access below (TMA
+  // loads and stores) comes after the previous kernel on the stream has completed.
+  pdl_launch_dependents();
+  pdl_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -412,7 +416,7 @@ struct Bf16Variant {
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
     cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
@@ -421,8 +425,10 @@ struct Bf16Variant {
     attr[0].val.clusterDim.x = CG;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = opt.pdl ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tc, p);
     if (e != cudaSuccess) {
       cudaGetLastError();

@@ -429,6 +429,10 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   x.tmem_base = *tmem_slot;
+  // Set-up is done: the next kernel may start its own. Every global access below (TMA
+  // loads and stores) comes after the previous kernel on the stream has completed.
+  pdl_launch_dependents();
+  pdl_wait();
 
   // One branch per warpgroup, each with one register-limit change for all its warps: the
   // epilogue warpgroup takes the registers that warpgroups 0 and 2 give up. Each branch
@@ -559,7 +563,7 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
                                                info->l2_bytes);
 
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * 2), 1, 1);
   cfg.blockDim = dim3(NL::NUM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = NL::SMEM_BYTES;
@@ -568,8 +572,10 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = opt.pdl ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kNvfp4Kernel, ta, tb, tbh, tsa, tsb, tc, p);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -42,6 +42,7 @@ struct RunOptions {
   int group_m = 0;
   int max_clusters = 0;
   int tail_split = 1;
+  int pdl = 1;  // programmatic stream serialization on the launch
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
 };
@@ -50,10 +51,10 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
                   const RunOptions& opt);
 int run_gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                            int M, int N, int K, cudaStream_t stream, const RunOptions& opt);
-int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream);
+int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream, int pdl = 1);
 // Both matrices of a GEMM in one launch (rows0 + rows1 row blocks).
 int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int pdl = 1);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).
 int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,

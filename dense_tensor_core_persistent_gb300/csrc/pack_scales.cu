@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "host_common.h"
+#include "ptx.cuh"
 #include "schedule.h"
 
 namespace dtcp {
@@ -42,6 +43,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_scales_kernel(const uint8_t
   const int rb = second ? static_cast<int>(blockIdx.y) - rb0 : static_cast<int>(blockIdx.y);
   const int j0 = blockIdx.x * kPackSteps;
   const int nj = min(kPackSteps, ksteps - j0);
+  pdl_launch_dependents();
+  pdl_wait();  // the scales may come from the previous kernel on the stream
   for (int i = threadIdx.x; i < kPackRows * kPackSteps; i += kPackThreads) {
     const int r = i / kPackSteps, w = i % kPackSteps;
     const int row = rb * kPackRows + r;
@@ -60,20 +63,31 @@ __global__ void __launch_bounds__(kPackThreads) pack_scales_kernel(const uint8_t
 }
 
 int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, int pdl) {
   const int ksteps = K / 64;
   const int blocks_y = ceil_div(rows0, kPackRows) + ceil_div(rows1, kPackRows);
-  const dim3 grid(static_cast<unsigned>(ceil_div(ksteps, kPackSteps)), static_cast<unsigned>(blocks_y));
-  pack_scales_kernel<<<grid, kPackThreads, 0, stream>>>(static_cast<const uint8_t*>(SF0), static_cast<uint8_t*>(out0),
-                                                        rows0, static_cast<const uint8_t*>(SF1),
-                                                        static_cast<uint8_t*>(out1), rows1, K / 16, ksteps);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(ksteps, kPackSteps)), static_cast<unsigned>(blocks_y), 1);
+  cfg.blockDim = dim3(kPackThreads, 1, 1);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, pack_scales_kernel, static_cast<const uint8_t*>(SF0), static_cast<uint8_t*>(out0), rows0,
+                         static_cast<const uint8_t*>(SF1), static_cast<uint8_t*>(out1), rows1, K / 16, ksteps);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
   count_launch();
   return GEMM_OK;
 }
 
-int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream) {
-  return run_pack_scales2(SF, SF_blocked, rows, nullptr, nullptr, 0, K, stream);
+int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream, int pdl) {
+  return run_pack_scales2(SF, SF_blocked, rows, nullptr, nullptr, 0, K, stream, pdl);
 }
 
 }  // namespace dtcp

@@ -204,6 +204,17 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel on the stream (launched with programmatic stream serialization)
+// start its CTAs' set-up; its global accesses still wait for this grid (pdl_wait).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory operations
+// are visible; a no-op for a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- register reallocation
 
 // Per-warpgroup register limits: every warp of a warpgroup executes the same call. The

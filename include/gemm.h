@@ -201,7 +201,10 @@ typedef struct {
                                  nobody arrives on (exercises the timeout path) */
     int no_tail_split;   /* 0: when the last wave of a persistent grid is at most half full,
                             its tiles are computed as two N-halves each; 1: never */
-    int reserved[3];     /* must be zero */
+    int no_pdl;          /* 0: launch with programmatic stream serialization (the kernel's
+                            set-up overlaps the end of the previous kernel on the stream;
+                            every global access waits for that kernel); 1: plain launch */
+    int reserved[2];     /* must be zero */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
@@ -209,7 +212,7 @@ int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, voi
                  const gemm_options_t* options);
 
 /* gemm_nvfp4 with explicit options (only persistent, group_m, max_clusters,
- * wait_limit_us, debug_flags and no_tail_split apply; kernel must be
+ * wait_limit_us, debug_flags, no_tail_split and no_pdl apply; kernel must be
  * GEMM_KERNEL_DEFAULT). */
 int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                   int M, int N, int K, void* stream, const gemm_options_t* options);
@@ -244,6 +247,24 @@ int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_by
 
 /* Number of kernel launches this library has issued in this process (all devices). */
 unsigned long long gemm_launch_count(void);
+
+/*
+ * gemm_measure_mma_rate -- measures, on the current device, the throughput of one of the
+ * two tensor-core MMA kinds the GEMMs issue, as FLOP per SM clock: one CTA pair per two
+ * SMs issues 8192 back-to-back M = 256, N = 256 MMAs (cta_group::2) into one TMEM
+ * accumulator from shared memory, timed with the SM clock (the second of two launches).
+ *   kind: GEMM_MMA_BF16  -- kind::f16, BF16 operands, K = 16 per instruction;
+ *         GEMM_MMA_NVFP4 -- kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 operands with
+ *                           UE4M3 scales, K = 64 per instruction.
+ *   *flop_per_clock_per_sm: the result (2 * M * N * K per instruction, per SM, per clock).
+ * It is the ceiling a kernel made of these instructions can reach per clock; multiplied
+ * by the SM count and clock it gives TFLOP/s. Synchronous: it runs on a private stream
+ * and waits for it. Device memory: none beyond the library's static device arrays.
+ * Errors: GEMM_ERR_INVALID_ARG (unknown kind, null pointer), device errors as for the
+ * GEMMs, GEMM_ERR_TIMEOUT if the MMAs did not complete within 2 s.
+ */
+enum { GEMM_MMA_BF16 = 0, GEMM_MMA_NVFP4 = 1 };
+int gemm_measure_mma_rate(int kind, double* flop_per_clock_per_sm);
 
 #ifdef __cplusplus
 }

@@ -110,3 +110,10 @@ def test_group_choice():
     gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 74, L2)
     assert 1 <= gl < 9
     assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 74, L2) >= 1
+
+
+def test_mma_rate_argument_errors():
+    import ctypes
+    out = ctypes.c_double(0.0)
+    assert g.lib().gemm_measure_mma_rate(7, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.lib().gemm_measure_mma_rate(g.GEMM_MMA_BF16, None) == g.GEMM_ERR_INVALID_ARG

@@ -221,3 +221,45 @@ def test_bounded_wait_reports_timeout_and_context_survives(kernel):
     A2, B2 = si.bf16_problem(1, 256, 256, 256)
     assert_bf16_close(run(A2, B2, kernel=kernel), oracle.gemm_bf16(A2, B2), 256, "after timeout")
     assert g.get_device_status()[0] == g.GEMM_OK
+
+
+def test_mma_instruction_rates():
+    """The two MMA kinds the kernels issue, measured on this GPU (FLOP per SM clock). BF16:
+    the documented 8192 (M=256 N=256 K=16 in 128 cycles per SM pair). The FP4 block-scaled
+    kind is a multiple of it; the kernels' roofline notes depend on that ratio."""
+    bf16 = g.measure_mma_rate(g.GEMM_MMA_BF16)
+    fp4 = g.measure_mma_rate(g.GEMM_MMA_NVFP4)
+    assert 0.9 * 8192 <= bf16 <= 1.02 * 8192, bf16
+    assert 3.5 <= fp4 / bf16 <= 6.5, (bf16, fp4)
+    assert g.get_device_status()[0] == g.GEMM_OK
+
+
+@pytest.mark.parametrize("no_pdl", [0, 1])
+def test_dependent_launches_on_one_stream(no_pdl):
+    """Back-to-back GEMMs where each reads what the previous one wrote (read after write)
+    and writes what the previous one read (write after read). With programmatic dependent
+    launch the next kernel starts early, so its global accesses must still wait."""
+    M = N = K = 512
+    opts = g.options(no_pdl=no_pdl)
+    A, B = si.bf16_problem(90, M, N, K, kind="int", device=DEV)
+    _, D = si.bf16_problem(91, M, N, K, kind="int", device=DEV)
+    s = torch.cuda.Stream(device=DEV)
+    X = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    A2 = A.clone()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g.gemm_bf16(A, B, X, M, N, K, stream=s, opts=opts)       # X = A B^T
+            g.gemm_bf16(X, D, Y, M, N, K, stream=s, opts=opts)       # reads X
+            g.gemm_bf16(D, B, A2, M, N, K, stream=s, opts=opts)      # overwrites A2 ...
+            g.gemm_bf16(A2, B, X, M, N, K, stream=s, opts=opts)      # ... then reads it, writes X
+    s.synchronize()
+    X_ref = oracle.gemm_bf16(A.cpu(), B.cpu())
+    # the intermediate results enter the next GEMM as BF16 bit patterns (one rounding of the
+    # exact FP32 sums: integer inputs keep every partial sum exact)
+    Y_ref = oracle.gemm_bf16(oracle.round_bf16(X_ref), D.cpu())
+    A2_ref = oracle.gemm_bf16(D.cpu(), B.cpu())
+    X2_ref = oracle.gemm_bf16(oracle.round_bf16(A2_ref), B.cpu())
+    assert_bf16_close(bits(Y), Y_ref, K, "Y = (A B^T) D^T")
+    assert_bf16_close(bits(A2), A2_ref, K, "A2 = D B^T")
+    assert_bf16_close(bits(X), X2_ref, K, "X = A2 B^T")

@@ -214,3 +214,23 @@ def test_launches_per_call():
     g.gemm_nvfp4_blocked(a, pa, b, pb, C, M, N, K)
     torch.cuda.synchronize()
     assert g.launch_count() == before + 1
+
+
+@pytest.mark.parametrize("no_pdl", [0, 1])
+def test_back_to_back_calls_on_one_stream(no_pdl):
+    """Consecutive gemm_nvfp4 calls on one stream: each packs its scales into a pooled
+    workspace that the previous call's GEMM may have just released, and with programmatic
+    dependent launch each kernel starts before the previous one ends."""
+    M, N, K = 384, 512, 1024
+    probs = [si.nvfp4_problem(60 + i, M, N, K, device=DEV) for i in range(4)]
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(4)]
+    opts = g.options(no_pdl=no_pdl)
+    s = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()
+    for rep in range(2):
+        for (a, sfa, b, sfb), out in zip(probs, outs):
+            g.gemm_nvfp4(a, sfa, b, sfb, out, M, N, K, stream=s, opts=opts)
+    s.synchronize()
+    for (a, sfa, b, sfb), out in zip(probs, outs):
+        ref = oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu())
+        assert_nvfp4_close(bits(out), ref, "back to back")
