@@ -174,7 +174,8 @@ def max_over_ranks(x: float, world: int) -> float:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -282,7 +283,7 @@ def run_reference(args, cfg, world, rank):
     ins_cpu = make_sample_inputs(cfg, sample_rows)
     rng = np.random.default_rng(cfg["seed"])
     total = args.steps + args.warmup
-    budget = 120.0
+    budget = args.ref_seconds
     cal = 256
     rows, cols = rng.integers(0, sample_rows, cal), rng.integers(0, N, cal)
     oracle_at(cfg, ins_cpu, rows, cols)
@@ -507,6 +508,8 @@ def main():
     ap.add_argument("--scales", default="blocked", choices=["blocked", "rowmajor"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="--impl reference: host seconds for warm-up + timed steps together")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -42,6 +42,7 @@ struct Bf16Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
+  int zigzag;  // 1: a cluster's odd-numbered tiles walk K downwards
 };
 
 template <int CG, int STAGES, int ATOMS>
@@ -146,18 +147,23 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters) {
+      int it = 0;
+      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
         const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
         const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
         const bool half = w.half >= 0;
+        const bool down = p.zigzag && (it & 1);
         const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
         const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
                                                         : static_cast<int>(rank) * L::B_ROWS);
         const CUtensorMap* map_b = half ? &tmap_b_half : &tmap_b;
         const uint32_t atom_bytes = L::A_ATOM_BYTES + (half ? L::B_ATOM_BYTES / 2 : L::B_ATOM_BYTES);
         for (int kb = 0; kb < p.k_iters; ++kb) {
-          // swizzle-row columns of this stage that hold any of K (the last stage may hold fewer)
-          const int atoms = min(ATOMS, (p.K - kb * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K);
+          // K block of this stage: every other tile of the cluster walks K downwards, so
+          // it starts on the K blocks the previous wave of tiles read last (still in L2)
+          const int kblk = down ? p.k_iters - 1 - kb : kb;
+          // swizzle-row columns of this stage that hold any of K (the last block may hold fewer)
+          const int atoms = min(ATOMS, (p.K - kblk * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K);
           const uint32_t stage_bytes = atom_bytes * static_cast<uint32_t>(atoms);
           // First pass over the ring: parity 1 of a fresh barrier counts as complete.
           if (!wait_phase(bar_empty + 8 * stage, phase ^ 1u, wctx, status_code(kRoleProducer, stage))) {
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           if constexpr (CG == 1) {
             mbar_arrive_expect_tx(full, stage_bytes);
             for (int a = 0; a < atoms; ++a) {
-              const int x = kb * L::BLOCK_K + a * L::ATOM_K;
+              const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
               tma_load_2d(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full);
               tma_load_2d(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full);
             }
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
             const uint32_t full_leader = mapa_shared(full, 0);
             if (rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
             for (int a = 0; a < atoms; ++a) {
-              const int x = kb * L::BLOCK_K + a * L::ATOM_K;
+              const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
               tma_load_2d_pair(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full_leader);
               tma_load_2d_pair(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full_leader);
             }
@@ -213,14 +219,16 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + slot * L::ACC_COLS;
+        const bool down = p.zigzag && (it & 1);  // the producer's K order for this tile
         for (int kb = 0; kb < p.k_iters; ++kb) {
+          const int kblk = down ? p.k_iters - 1 - kb : kb;
           if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           // MMAs of the swizzle-row columns that hold any of K (all of them but in a ragged last stage)
-          const int ksteps = min(L::KSTEPS, (p.K - kb * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K * (L::ATOM_K / L::UMMA_K));
+          const int ksteps = min(L::KSTEPS, (p.K - kblk * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K * (L::ATOM_K / L::UMMA_K));
 #pragma unroll
           for (int kk = 0; kk < L::KSTEPS; ++kk) {
             if (kk < ksteps) {
@@ -398,6 +406,7 @@ struct Bf16Variant {
     p.status = device_status_word(device);
     p.wait_limit_ns = opt.wait_limit_ns;
     p.debug_flags = opt.debug_flags;
+    p.zigzag = 1;
     if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
     const int max_clusters = max_active_clusters(device);

@@ -55,6 +55,7 @@ struct Nvfp4Params {
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
   int mma_group;  // stages the MMA issuer takes per scale-ready wait (1 .. STAGES)
+  int zigzag;     // 1: a cluster's odd-numbered tiles walk K downwards
 };
 
 template <int STAGES>
@@ -134,10 +135,14 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
   const int ksteps = p.K / L::UMMA_K;  // 512-byte scale blocks per 128 rows
   uint32_t stage = 0, phase = 0;
   bool ok = true;
-  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters) {
+  int it = 0;
+  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
     const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
     const bool half = w.half >= 0;
+    // every other tile of the cluster walks K downwards, so it starts on the K blocks the
+    // previous wave of tiles read last (still in L2)
+    const bool down = p.zigzag && (it & 1);
     const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(x.rank) * L::BLOCK_M;
     const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(x.rank) * (L::B_ROWS / 2)
                                                     : static_cast<int>(x.rank) * L::B_ROWS);
@@ -153,8 +158,9 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
       }
       const uint32_t full = x.bar_full + 8 * stage;
       const uint32_t full_leader = mapa_shared(full, 0);
-      const int kx = kb * (L::BLOCK_K / 2);
-      const int ky = kb * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
+      const int kblk = down ? p.k_iters - 1 - kb : kb;
+      const int kx = kblk * (L::BLOCK_K / 2);
+      const int ky = kblk * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
       if (x.warp == L::WARP_PROD_A) {
         // one arrival with the bytes of both CTAs; the other loads may land before it
         if (x.rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
@@ -543,6 +549,7 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.wait_limit_ns = opt.wait_limit_ns;
   p.debug_flags = opt.debug_flags;
   p.mma_group = 2;  // measured: 1 -> 15% slower, 3 -> 4% slower (the wait for the third stage)
+  p.zigzag = 1;
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = max_active_clusters(device);
