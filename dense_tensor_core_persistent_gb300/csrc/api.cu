@@ -124,7 +124,7 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
 }
 
 int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
-                   const uint64_t strides_bytes[2], const uint32_t box[3]) {
+                   const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return GEMM_ERR_DRIVER;
   const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
@@ -132,7 +132,7 @@ int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base
   const cuuint32_t b[3] = {box[0], box[1], box[2]};
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, b, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
 }

@@ -26,9 +26,10 @@ const DeviceInfo* current_device_info(int* device, int* err);
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
                    uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                    CUtensorMapSwizzle swizzle);
-// 3-D map, no swizzle: dims[0] innermost (elements), strides of dims 1 and 2 in bytes.
+// 3-D map: dims[0] innermost (elements), strides of dims 1 and 2 in bytes.
 int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
-                   const uint64_t strides_bytes[2], const uint32_t box[3]);
+                   const uint64_t strides_bytes[2], const uint32_t box[3],
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 // Device address of the process-wide status word on the current device.
 unsigned* device_status_word(int device);
