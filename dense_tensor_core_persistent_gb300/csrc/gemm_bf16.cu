@@ -1,7 +1,9 @@
 // gemm_bf16.cu -- BF16 C = A * B^T on sm_103a tensor cores (tcgen05), FP32 accumulation.
 //
 // One persistent, warp-specialised kernel template:
-//   warp 0      TMA producer: fills an S-stage shared-memory ring with A and B K-slices
+//   warp 0      TMA producer of A: fills an S-stage shared-memory ring with A K-slices and
+//               arms the stage's full barrier
+//   warp 6      TMA producer of B (its own thread, so a stage's loads go out sooner)
 //   warp 1      MMA issuer (one thread of the pair's leader CTA) + TMEM allocator
 //   warps 2..5  epilogue: TMEM -> registers -> BF16 -> swizzled smem -> TMA store
 // CG = 1: one CTA computes a 128 x 256 tile (MMA M = 128).
@@ -65,7 +67,8 @@ struct Bf16Layout {
   static constexpr int EPI_WARPS = 4;
   static constexpr int EPI_BUFS = 2;
   static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;  // 32 rows x 64 BF16 columns (one swizzle row each)
-  static constexpr int NUM_THREADS = 32 * (2 + EPI_WARPS);
+  static constexpr int WARP_PROD_B = 2 + EPI_WARPS;  // warp 6
+  static constexpr int NUM_THREADS = 32 * (3 + EPI_WARPS);
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -142,8 +145,9 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
   pdl_launch_dependents();
   pdl_wait();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == L::WARP_PROD_B) {
+    // ------------------------------------------------------------ TMA producers (A: warp 0, B)
+    const bool load_a = warp == 0;
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -173,20 +177,22 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           const uint32_t full = bar_full + 8 * stage;
           const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
           const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
+          // The A producer arms the barrier with the stage's bytes (of both CTAs for a pair);
+          // the B loads may complete before that arrival, the phase cannot.
           if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(full, stage_bytes);
+            if (load_a) mbar_arrive_expect_tx(full, stage_bytes);
             for (int a = 0; a < atoms; ++a) {
               const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
-              tma_load_2d(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full);
-              tma_load_2d(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full);
+              if (load_a) tma_load_2d(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full);
+              else tma_load_2d(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full);
             }
           } else {
             const uint32_t full_leader = mapa_shared(full, 0);
-            if (rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
+            if (load_a && rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
             for (int a = 0; a < atoms; ++a) {
               const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
-              tma_load_2d_pair(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full_leader);
-              tma_load_2d_pair(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full_leader);
+              if (load_a) tma_load_2d_pair(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full_leader);
+              else tma_load_2d_pair(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full_leader);
             }
           }
           if (++stage == STAGES) {
@@ -265,7 +271,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < 2 + L::EPI_WARPS) {
     // ------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;  // this warp may access TMEM lanes 32q .. 32q+31
     const uint32_t epi = warp - 2u;
