@@ -57,8 +57,6 @@ struct Nvfp4Params {
   unsigned debug_flags;
   int mma_group;  // stages the MMA issuer takes per scale-ready wait (1 .. STAGES)
   int zigzag;     // 1: a cluster's odd-numbered tiles walk K downwards
-  int sf_issue_order;  // 1: scale-ready means the copies are issued (tensor-pipe order), not done
-  int relaxed_release;  // 1: the epilogue frees TMEM with a relaxed (not release) arrive
 };
 
 template <int STAGES>
@@ -212,16 +210,12 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
     tmem_cp_32x128b_warpx4<2>(col + 4 * c, sfa);
     tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * c, sfb);
     tmem_cp_32x128b_warpx4<2>(col + 20 + 8 * c, umma_desc_advance(sfb, L::SFB_BYTES / 2));
-    if (p.sf_issue_order) {
-      // tcgen05.cp and tcgen05.mma execute in issue order on the pair's tensor pipe: the
-      // MMAs need only be issued after these copies, which the fence and the barrier
-      // (arrive here, wait and fence::after_thread_sync in the MMA thread) establish.
-      // The MMA thread does not wait for the copies to complete.
-      tc_fence_before_sync();
-      mbar_arrive_local(x.bar_sfready + 8 * stage);
-    } else {
-      mma_commit_pair_multicast(x.bar_sfready + 8 * stage, 0x1);
-    }
+    // tcgen05.cp and tcgen05.mma execute in issue order on the pair's tensor pipe: the MMAs
+    // need only be issued after these copies, which the fence and the barrier (arrive here,
+    // wait and fence::after_thread_sync in the MMA thread) establish. The MMA thread does
+    // not wait for the copies to complete (a tcgen05.commit here would make it: -2.4%).
+    tc_fence_before_sync();
+    mbar_arrive_local(x.bar_sfready + 8 * stage);
     if (++stage == STAGES) {
       stage = 0;
       phase ^= 1u;
@@ -348,10 +342,7 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
     // this warp's part of the accumulator is in registers: release TMEM, then convert and store
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) {
-      if (p.relaxed_release) mbar_arrive_cluster_relaxed(tempty_leader);
-      else mbar_arrive_cluster(tempty_leader);
-    }
+    if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);  // orders tcgen05 work only
     if (live) {
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -568,8 +559,6 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.debug_flags = opt.debug_flags;
   p.mma_group = 2;  // measured: 1 -> 15% slower, 3 -> 4% slower (the wait for the third stage)
   p.zigzag = 1;
-  p.sf_issue_order = 1;
-  p.relaxed_release = 1;
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = max_active_clusters(device);
