@@ -162,6 +162,15 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
                                                         : static_cast<int>(rank) * L::B_ROWS);
         const CUtensorMap* map_b = half ? &tmap_b_half : &tmap_b;
         const uint32_t atom_bytes = L::A_ATOM_BYTES + (half ? L::B_ATOM_BYTES / 2 : L::B_ATOM_BYTES);
+        // Straight-line loop body: this producer's operand, map and row are fixed for the tile,
+        // the ring position advances by selects (each taken branch costs the thread cycles).
+        const uint32_t dst0 = base + (load_a ? L::OFF_A : L::OFF_B);
+        const uint32_t atom_stride = load_a ? L::A_ATOM_BYTES : L::B_ATOM_BYTES;
+        const uint32_t stage_stride = load_a ? L::A_BYTES : L::B_BYTES;
+        const CUtensorMap* map = load_a ? &tmap_a : map_b;
+        const int row = load_a ? a_row : b_row;
+        const bool arm = load_a && (CG == 1 || rank == 0);
+#pragma unroll 2
         for (int kb = 0; kb < p.k_iters; ++kb) {
           // K block of this stage: every other tile of the cluster walks K downwards, so
           // it starts on the K blocks the previous wave of tiles read last (still in L2)
@@ -175,30 +184,26 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
             break;
           }
           const uint32_t full = bar_full + 8 * stage;
-          const uint32_t sa = base + L::OFF_A + stage * L::A_BYTES;
-          const uint32_t sb = base + L::OFF_B + stage * L::B_BYTES;
+          const uint32_t dst = dst0 + stage * stage_stride;
+          const int x0 = kblk * L::BLOCK_K;
           // The A producer arms the barrier with the stage's bytes (of both CTAs for a pair);
           // the B loads may complete before that arrival, the phase cannot.
-          if constexpr (CG == 1) {
-            if (load_a) mbar_arrive_expect_tx(full, stage_bytes);
-            for (int a = 0; a < atoms; ++a) {
-              const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
-              if (load_a) tma_load_2d(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full);
-              else tma_load_2d(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full);
+          if (arm) mbar_arrive_expect_tx(full, (CG == 2 ? 2u : 1u) * stage_bytes);
+          const uint32_t target = CG == 2 ? mapa_shared(full, 0) : full;
+          if (atoms == ATOMS) {
+#pragma unroll
+            for (int a = 0; a < ATOMS; ++a) {
+              if constexpr (CG == 1) tma_load_2d(dst + a * atom_stride, map, x0 + a * L::ATOM_K, row, target);
+              else tma_load_2d_pair(dst + a * atom_stride, map, x0 + a * L::ATOM_K, row, target);
             }
           } else {
-            const uint32_t full_leader = mapa_shared(full, 0);
-            if (load_a && rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
             for (int a = 0; a < atoms; ++a) {
-              const int x = kblk * L::BLOCK_K + a * L::ATOM_K;
-              if (load_a) tma_load_2d_pair(sa + a * L::A_ATOM_BYTES, &tmap_a, x, a_row, full_leader);
-              else tma_load_2d_pair(sb + a * L::B_ATOM_BYTES, map_b, x, b_row, full_leader);
+              if constexpr (CG == 1) tma_load_2d(dst + a * atom_stride, map, x0 + a * L::ATOM_K, row, target);
+              else tma_load_2d_pair(dst + a * atom_stride, map, x0 + a * L::ATOM_K, row, target);
             }
           }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          stage = stage + 1 == STAGES ? 0u : stage + 1;
+          phase = stage == 0 ? phase ^ 1u : phase;
         }
       }
       if (!ok) settle_after_abort();
@@ -214,7 +219,6 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
       if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
       int it = 0;
       const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
-      uint64_t a_desc = a_desc0, b_desc = b_desc0;  // advanced with the ring position
       for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
         const uint32_t idesc = (i >= p.num_tiles - p.split_tiles) ? IDESC_HALF : IDESC_FULL;
         const uint32_t slot = static_cast<uint32_t>(it) & 1u;
@@ -226,6 +230,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + slot * L::ACC_COLS;
         const bool down = p.zigzag && (it & 1);  // the producer's K order for this tile
+        // Straight-line loop body: descriptors follow from the ring position, which advances
+        // by selects; a full stage issues its MMAs without per-MMA tests (each taken branch
+        // costs this thread cycles).
+#pragma unroll 2
         for (int kb = 0; kb < p.k_iters; ++kb) {
           const int kblk = down ? p.k_iters - 1 - kb : kb;
           if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
@@ -233,12 +241,21 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
+          const uint64_t a_desc = umma_desc_advance(a_desc0, stage * L::A_BYTES);
+          const uint64_t b_desc = umma_desc_advance(b_desc0, stage * L::B_BYTES);
           // MMAs of the swizzle-row columns that hold any of K (all of them but in a ragged last stage)
           const int ksteps = min(L::KSTEPS, (p.K - kblk * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K * (L::ATOM_K / L::UMMA_K));
+          if (ksteps == L::KSTEPS) {
 #pragma unroll
-          for (int kk = 0; kk < L::KSTEPS; ++kk) {
-            if (kk < ksteps) {
+            for (int kk = 0; kk < L::KSTEPS; ++kk) {
               // column kk / 4 of the stage, then 32 bytes per MMA inside its 128-byte swizzle row
+              const uint32_t koff_a = (kk / 4) * L::A_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
+              const uint32_t koff_b = (kk / 4) * L::B_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
+              mma_f16<CG>(d_tmem, umma_desc_advance(a_desc, koff_a), umma_desc_advance(b_desc, koff_b), idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+            }
+          } else {
+            for (int kk = 0; kk < ksteps; ++kk) {
               const uint32_t koff_a = (kk / 4) * L::A_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
               const uint32_t koff_b = (kk / 4) * L::B_ATOM_BYTES + (kk % 4) * L::UMMA_K * 2;
               mma_f16<CG>(d_tmem, umma_desc_advance(a_desc, koff_a), umma_desc_advance(b_desc, koff_b), idesc,
@@ -248,15 +265,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           // Release the stage when these MMAs have read it; never wait here.
           if constexpr (CG == 1) mma_commit_local(bar_empty + 8 * stage);
           else mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-            a_desc = a_desc0;
-            b_desc = b_desc0;
-          } else {
-            a_desc = umma_desc_advance(a_desc, L::A_BYTES);
-            b_desc = umma_desc_advance(b_desc, L::B_BYTES);
-          }
+          stage = stage + 1 == STAGES ? 0u : stage + 1;
+          phase = stage == 0 ? phase ^ 1u : phase;
         }
         if (!ok) break;
         if constexpr (CG == 1) mma_commit_local(bar_tfull + 8 * slot);

@@ -55,7 +55,6 @@ struct Nvfp4Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
-  int mma_group;  // stages the MMA issuer takes per scale-ready wait (1 .. STAGES)
   int zigzag;     // 1: a cluster's odd-numbered tiles walk K downwards
 };
 
@@ -151,31 +150,45 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
     // a half item loads half the B rows; the scales of the whole tile are loaded either way
     const uint32_t stage_bytes = L::STAGE_BYTES - (half ? L::B_BYTES / 2 : 0);
     const int sfa_block = (a_row / 128) * ksteps;
-    for (int kb = 0; kb < p.k_iters; ++kb) {
-      // First pass over the ring: parity 1 of a fresh barrier counts as complete.
-      if (!wait_phase_inline(x.bar_empty + 8 * stage, phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | stage))) {
-        ok = false;
-        break;
+    // One straight-line loop per producer (the ring position and the K block advance by
+    // selects): A and B issue one 2-D copy per stage, the scale producer a 2-D and a 3-D one.
+    if (x.warp != L::WARP_PROD_SF) {
+      static_assert(L::A_BYTES == L::B_BYTES, "A and B stages share one stride");
+      const bool is_a = x.warp == L::WARP_PROD_A;
+      const bool arm = is_a && x.rank == 0;  // one arrival with the bytes of both CTAs
+      const uint32_t dst0 = x.base + (is_a ? L::OFF_A : L::OFF_B);
+      const CUtensorMap* map = is_a ? tmap_a : map_b;
+      const int row = is_a ? a_row : b_row;
+#pragma unroll 2
+      for (int kb = 0; kb < p.k_iters; ++kb) {
+        // First pass over the ring: parity 1 of a fresh barrier counts as complete.
+        if (!wait_phase_inline(x.bar_empty + 8 * stage, phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | stage))) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = x.bar_full + 8 * stage;
+        const int kblk = down ? p.k_iters - 1 - kb : kb;
+        // the other loads may land before the arrival
+        if (arm) mbar_arrive_expect_tx(full, 2 * stage_bytes);
+        tma_load_2d_pair(dst0 + stage * L::A_BYTES, map, kblk * (L::BLOCK_K / 2), row, mapa_shared(full, 0));
+        stage = stage + 1 == STAGES ? 0u : stage + 1;
+        phase = stage == 0 ? phase ^ 1u : phase;
       }
-      const uint32_t full = x.bar_full + 8 * stage;
-      const uint32_t full_leader = mapa_shared(full, 0);
-      const int kblk = down ? p.k_iters - 1 - kb : kb;
-      const int kx = kblk * (L::BLOCK_K / 2);
-      const int ky = kblk * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
-      if (x.warp == L::WARP_PROD_A) {
-        // one arrival with the bytes of both CTAs; the other loads may land before it
-        if (x.rank == 0) mbar_arrive_expect_tx(full, 2 * stage_bytes);
-        tma_load_2d_pair(x.base + L::OFF_A + stage * L::A_BYTES, tmap_a, kx, a_row, full_leader);
-      } else if (x.warp == L::WARP_PROD_B) {
-        tma_load_2d_pair(x.base + L::OFF_B + stage * L::B_BYTES, map_b, kx, b_row, full_leader);
-      } else {
+    } else {
+#pragma unroll 2
+      for (int kb = 0; kb < p.k_iters; ++kb) {
+        if (!wait_phase_inline(x.bar_empty + 8 * stage, phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | stage))) {
+          ok = false;
+          break;
+        }
+        const uint32_t full_leader = mapa_shared(x.bar_full + 8 * stage, 0);
+        const int kblk = down ? p.k_iters - 1 - kb : kb;
+        const int ky = kblk * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
         tma_load_2d_pair(x.base + L::OFF_SFA + stage * L::SFA_BYTES, tmap_sfa, 0, sfa_block + ky, full_leader);
         // both 128-row blocks of the tile's SFB (row blocks 2n and 2n+1), steps ky .. ky+3
         tma_load_3d_pair(x.base + L::OFF_SFB + stage * L::SFB_BYTES, tmap_sfb, 0, ky, tc.n_blk * 2, full_leader);
-      }
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
+        stage = stage + 1 == STAGES ? 0u : stage + 1;
+        phase = stage == 0 ? phase ^ 1u : phase;
       }
     }
   }
@@ -196,16 +209,19 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
   const long long total = static_cast<long long>(x.my_items > 0 ? x.my_items : 0) * p.k_iters;
   const uint64_t sfa0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFA, 128), c * L::SF_BLOCK);
   const uint64_t sfb0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFB, 128), c * L::SF_BLOCK);
-  uint64_t sfa = sfa0, sfb = sfb0;
   const uint32_t col0 = x.tmem_base + L::SF_TMEM_COL0;
-  uint32_t col = col0;
   uint32_t stage = 0, phase = 0;
   bool ok = true;
+  // straight-line loop body: the ring position advances by selects
+#pragma unroll 2
   for (long long g = 0; g < total; ++g) {
     if (!wait_phase_inline(x.bar_full + 8 * stage, phase, x.wctx, status_code(kRoleScales, 0x300 + stage))) {
       ok = false;
       break;
     }
+    const uint64_t sfa = umma_desc_advance(sfa0, stage * L::SFA_BYTES);
+    const uint64_t sfb = umma_desc_advance(sfb0, stage * L::SFB_BYTES);
+    const uint32_t col = col0 + stage * L::SF_COLS;
     tc_fence_after_sync();
     tmem_cp_32x128b_warpx4<2>(col + 4 * c, sfa);
     tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * c, sfb);
@@ -216,22 +232,37 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
     // not wait for the copies to complete (a tcgen05.commit here would make it: -2.4%).
     tc_fence_before_sync();
     mbar_arrive_local(x.bar_sfready + 8 * stage);
-    if (++stage == STAGES) {
-      stage = 0;
-      phase ^= 1u;
-      sfa = sfa0;
-      sfb = sfb0;
-      col = col0;
-    } else {
-      sfa = umma_desc_advance(sfa, L::SFA_BYTES);
-      sfb = umma_desc_advance(sfb, L::SFB_BYTES);
-      col += L::SF_COLS;
-    }
+    stage = stage + 1 == STAGES ? 0u : stage + 1;
+    phase = stage == 0 ? phase ^ 1u : phase;
   }
   if (!ok) settle_after_abort();
 }
 
 // ---------------------------------------------------------------- MMA issuer (leader)
+// The 4 MMAs of one stage and the commit that releases it when they have read it (shared
+// memory and TMEM scales). Descriptors and scale columns follow from the ring position.
+template <int STAGES>
+__device__ __forceinline__ void mma_stage(const Nvfp4Ctx& x, uint64_t a_desc0, uint64_t b_desc0, uint32_t sf_col0,
+                                          uint32_t idesc, uint32_t sfb_half_col, uint32_t stage, bool first) {
+  using L = Nvfp4Layout<STAGES>;
+  const uint64_t a_desc = umma_desc_advance(a_desc0, stage * L::A_BYTES);
+  const uint64_t b_desc = umma_desc_advance(b_desc0, stage * L::B_BYTES);
+  const uint32_t sf_col = sf_col0 + stage * L::SF_COLS;
+#pragma unroll
+  for (int j = 0; j < L::KSTEPS; ++j) {
+    const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
+    mma_nvf4<2>(x.tmem_base, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc, sf_col + 4 * j,
+                sf_col + 16 + 8 * j + sfb_half_col, (first && j == 0) ? 0u : 1u);
+  }
+  mma_commit_pair_multicast(x.bar_empty + 8 * stage, 0x3);
+}
+
+// Two stages per scale-ready wait: each copier commits its stages in order, and a commit
+// covers all earlier copies of its thread, so the scale-ready phase of the later stage
+// implies the earlier one's; the copiers copied each stage only after its full barrier, so
+// both stages' tiles are in shared memory too. The loop body is straight-line code (ring
+// position by selects, no inner loop): each taken branch in this thread's loop cost it
+// hundreds of cycles.
 template <int STAGES>
 __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x) {
   using L = Nvfp4Layout<STAGES>;
@@ -241,11 +272,8 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
   uint32_t stage = 0, phase = 0;
   bool ok = true;
   if (p.debug_flags & 1u) ok = wait_phase_inline(x.bar_never, 0, x.wctx, status_code(kRoleMma, 0xFFFF));
-  // Per-stage operand descriptors and scale columns, advanced with the ring position.
   const uint64_t a_desc0 = umma_desc_sw128(x.base + L::OFF_A), b_desc0 = umma_desc_sw128(x.base + L::OFF_B);
   const uint32_t sf_col0 = x.tmem_base + L::SF_TMEM_COL0;
-  uint64_t a_desc = a_desc0, b_desc = b_desc0;
-  uint32_t sf_col = sf_col0;
   int it = 0;
   for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
@@ -256,43 +284,30 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
       break;
     }
     tc_fence_after_sync();
-    for (int kb = 0; kb < p.k_iters;) {
-      // Several stages per wait where the tile has them. Each copier commits its stages in
-      // order, and a commit covers all earlier copies of its thread, so the scale-ready
-      // phase of a later stage implies the earlier ones'; the copiers copied each stage
-      // only after its full barrier, so the stages' tiles are in shared memory too.
-      const int n = min(p.mma_group, p.k_iters - kb);
-      uint32_t last = stage, last_phase = phase;
-      for (int u = 1; u < n; ++u)
-        if (++last == STAGES) {
-          last = 0;
-          last_phase ^= 1u;
-        }
-      if (!wait_phase_inline(x.bar_sfready + 8 * last, last_phase, x.wctx, status_code(kRoleMma, 0x200 + last))) {
+    const int pairs = p.k_iters >> 1;
+    int kb = 0;
+#pragma unroll 2
+    for (int q = 0; q < pairs; ++q, kb += 2) {
+      const uint32_t s1 = stage + 1 == STAGES ? 0u : stage + 1;
+      const uint32_t ph1 = s1 == 0 ? phase ^ 1u : phase;
+      if (!wait_phase_inline(x.bar_sfready + 8 * s1, ph1, x.wctx, status_code(kRoleMma, 0x200 + s1))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      for (int u = 0; u < n; ++u, ++kb) {
-#pragma unroll
-        for (int j = 0; j < L::KSTEPS; ++j) {
-          const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
-          mma_nvf4<2>(x.tmem_base, umma_desc_advance(a_desc, koff), umma_desc_advance(b_desc, koff), idesc,
-                      sf_col + 4 * j, sf_col + 16 + 8 * j + sfb_half_col, (kb | j) != 0 ? 1u : 0u);
-        }
-        // release the stage when these MMAs have read it (shared memory and TMEM scales)
-        mma_commit_pair_multicast(x.bar_empty + 8 * stage, 0x3);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-          a_desc = a_desc0;
-          b_desc = b_desc0;
-          sf_col = sf_col0;
-        } else {
-          a_desc = umma_desc_advance(a_desc, L::A_BYTES);
-          b_desc = umma_desc_advance(b_desc, L::B_BYTES);
-          sf_col += L::SF_COLS;
-        }
+      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, kb == 0);
+      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, s1, false);
+      stage = s1 + 1 == STAGES ? 0u : s1 + 1;
+      phase = stage == 0 ? ph1 ^ 1u : ph1;
+    }
+    if (ok && kb < p.k_iters) {  // an odd number of stages: the last one alone
+      if (!wait_phase_inline(x.bar_sfready + 8 * stage, phase, x.wctx, status_code(kRoleMma, 0x200 + stage))) {
+        ok = false;
+      } else {
+        tc_fence_after_sync();
+        mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, kb == 0);
+        stage = stage + 1 == STAGES ? 0u : stage + 1;
+        phase = stage == 0 ? phase ^ 1u : phase;
       }
     }
     if (!ok) break;
@@ -557,7 +572,6 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.status = device_status_word(device);
   p.wait_limit_ns = opt.wait_limit_ns;
   p.debug_flags = opt.debug_flags;
-  p.mma_group = 2;  // measured: 1 -> 15% slower, 3 -> 4% slower (the wait for the third stage)
   p.zigzag = 1;
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
