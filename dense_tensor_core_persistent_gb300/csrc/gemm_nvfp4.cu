@@ -9,25 +9,31 @@
 // Persistent CTA pairs (cta_group::2), a 256 x 256 output tile per pair, 256 K-elements
 // (128 bytes of codes per row, one 128-byte swizzle row) per pipeline stage. Every
 // barrier wait, TMA issue, tcgen05.cp and tcgen05.mma costs its issuing thread tens to
-// hundreds of cycles (a wait about 160, a copy about 56, an MMA about 60), and a stage
-// keeps the tensor pipe busy only 512 cycles, so the per-stage work is spread over
-// threads of different warps, each well under that budget:
+// hundreds of cycles (a wait about 50-150, a copy about 25, an MMA about 75, a taken
+// branch up to 200: the loops are straight-line code), and a stage keeps the tensor pipe
+// busy only 512 cycles, so the per-stage work is spread over threads of different warps,
+// each under that budget:
 //   warp 0      TMA producer of A (both CTAs); arms the leader's full barrier
 //   warp 1      TMA producer of B (both CTAs)
 //   warp 2      TMA producer of SFA (this CTA's 128 rows) and SFB (all 256 rows, one 3-D box)
+//               into the scale ring, whose slots the copiers' commits free
 //   warp 3      MMA issuer (leader CTA) + TMEM allocator: one scale-ready wait per two
 //               stages, 4 MMAs and a commit per stage
 //   warps 4..11 epilogue: warp 4 + 4h + q reads TMEM lanes 32q.. of accumulator columns
 //               128h..128h+127 into registers (four loads, one wait), releases TMEM, then
-//               converts to BF16 and stores through shared memory with TMA
+//               converts to BF16 and stores 32 x 16 tiles through a 1 KB staging buffer
+//               with TMA (small, so that shared memory holds a sixth stage)
 //   warps 12..15 scale copiers (leader CTA): copier c copies the scales of MMA c of every
 //               stage (SFA, SFB rows 0-127, SFB rows 128-255) and arrives on sf_ready as
 //               soon as the copies are issued (copies and MMAs run in issue order)
+// Shared memory: 6 A/B stages (32 KB each), a 4-slot scale ring (6 KB each) and 8 KB of C
+// staging: the A/B ring covers the ~1300-cycle load latency of a stage with two stages
+// to spare.
 // Warpgroups 0 and 3 give up registers (setmaxnreg) to the epilogue warpgroups 1 and 2,
 // which hold the whole 128 x 256 FP32 accumulator of a CTA in registers to free TMEM after
 // a single load latency (the one TMEM slot is the MMAs' only accumulator).
 // TMEM (512 columns): accumulator in columns 0..255 (one slot; the epilogue releases it as
-// soon as it has read it); a 5-deep scale ring after it, 48 columns per stage (16 for SFA:
+// soon as it has read it); the 5-slot scale ring after it, 48 columns per slot (16 for SFA:
 // 4 MMAs x 4 columns; 32 for SFB: 4 MMAs x 2 N-halves x 4 columns).
 // A last wave at most half full runs as N-halves of its tiles (N = 128 MMAs).
 //
@@ -74,6 +80,11 @@ struct Nvfp4Layout {
   static constexpr int SFA_BYTES = KSTEPS * SF_BLOCK;     // 2 KB: this CTA's 128 rows
   static constexpr int SFB_BYTES = 2 * KSTEPS * SF_BLOCK; // 4 KB: all 256 rows of the tile
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+  // The scales have shallower rings than A and B: stage g uses A/B slot g % STAGES, scale
+  // slot g % SF_SMEM_STAGES in shared memory (freed when its copies complete, well before
+  // the stage's MMAs) and g % SF_STAGES in TMEM (5 slots fit beside the accumulator).
+  static constexpr int SF_STAGES = STAGES < 5 ? STAGES : 5;
+  static constexpr int SF_SMEM_STAGES = STAGES < 4 ? STAGES : 4;
   static constexpr int ACC_COLS = BLOCK_N;
   static constexpr int SF_COLS = KSTEPS * 4 + KSTEPS * 8;  // 16 + 32 TMEM columns per stage
   static constexpr int SF_TMEM_COL0 = ACC_COLS;
@@ -86,24 +97,26 @@ struct Nvfp4Layout {
   static constexpr int NUM_THREADS = 32 * (COPY_WARP0 + COPY_WARPS);
   // registers per thread after setmaxnreg (the launch gives 65536 / 512 -> 128)
   static constexpr int REGS_LAUNCH = 128, REGS_LOW = 64, REGS_EPI = 184;
-  static constexpr int EPI_BUFS = 1;
-  static constexpr int EPI_BUF_BYTES = 32 * 64 * 2;
 
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
-  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
-  static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + SF_SMEM_STAGES * SFA_BYTES;
+  static constexpr int OFF_EPI = OFF_SFB + SF_SMEM_STAGES * SFB_BYTES;
+  // C staging per epilogue warp: 32 rows x 16 columns (one TMA store box)
+  static constexpr int EPI_COLS = 16;
+  static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF_BYTES;
   // full[S], empty[S], sf_ready[S], tmem_full, tmem_empty, never, drain
-  static constexpr int NUM_BARS = 3 * STAGES + 4;
+  // full[S], empty[S], sf_ready[S], sf_free[SF_SMEM_STAGES], tmem_full, tmem_empty, never, drain
+  static constexpr int NUM_BARS = 3 * STAGES + SF_SMEM_STAGES + 4;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
 
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
-  static_assert(SF_TMEM_COL0 + STAGES * SF_COLS <= TMEM_COLS, "scale ring does not fit in TMEM");
+  static_assert(SF_TMEM_COL0 + SF_STAGES * SF_COLS <= TMEM_COLS, "scale ring does not fit in TMEM");
   static_assert(A_BYTES + B_BYTES == 32768, "A+B tile bytes per CTA per stage");
   static_assert(STAGE_BYTES == 38912, "38 KB stage of a CTA pair kernel");
   static_assert(NUM_THREADS == 512 && REGS_LAUNCH * NUM_THREADS <= 65536, "launch register budget");
@@ -118,7 +131,7 @@ struct Nvfp4Ctx {
   uint32_t warp, lane, rank;
   int cluster_idx, num_clusters, my_items;
   uint32_t tmem_base;
-  uint32_t bar_full, bar_empty, bar_sfready, bar_tfull, bar_tempty, bar_never, bar_drain;
+  uint32_t bar_full, bar_empty, bar_sfready, bar_sffree, bar_tfull, bar_tempty, bar_never, bar_drain;
   WaitCtx wctx;
 };
 
@@ -134,6 +147,7 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
   if (x.lane != 0) return;
   const int ksteps = p.K / L::UMMA_K;  // 512-byte scale blocks per 128 rows
   uint32_t stage = 0, phase = 0;
+  uint32_t sf_stage = 0, sf_phase = 0;  // the scale producer's slot in the scale ring
   bool ok = true;
   int it = 0;
   for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
@@ -175,20 +189,23 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
         phase = stage == 0 ? phase ^ 1u : phase;
       }
     } else {
+      // The scale slot is free once the copies of the stage that used it have completed
+      // (the copiers commit to sf_free): earlier than that stage's MMAs.
 #pragma unroll 2
       for (int kb = 0; kb < p.k_iters; ++kb) {
-        if (!wait_phase_inline(x.bar_empty + 8 * stage, phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | stage))) {
+        if (!wait_phase_inline(x.bar_sffree + 8 * sf_stage, sf_phase ^ 1u, x.wctx, status_code(kRoleProducer, (x.warp << 8) | sf_stage))) {
           ok = false;
           break;
         }
         const uint32_t full_leader = mapa_shared(x.bar_full + 8 * stage, 0);
         const int kblk = down ? p.k_iters - 1 - kb : kb;
         const int ky = kblk * L::KSTEPS;  // scale blocks of this stage: 4 consecutive ones
-        tma_load_2d_pair(x.base + L::OFF_SFA + stage * L::SFA_BYTES, tmap_sfa, 0, sfa_block + ky, full_leader);
+        tma_load_2d_pair(x.base + L::OFF_SFA + sf_stage * L::SFA_BYTES, tmap_sfa, 0, sfa_block + ky, full_leader);
         // both 128-row blocks of the tile's SFB (row blocks 2n and 2n+1), steps ky .. ky+3
-        tma_load_3d_pair(x.base + L::OFF_SFB + stage * L::SFB_BYTES, tmap_sfb, 0, ky, tc.n_blk * 2, full_leader);
+        tma_load_3d_pair(x.base + L::OFF_SFB + sf_stage * L::SFB_BYTES, tmap_sfb, 0, ky, tc.n_blk * 2, full_leader);
         stage = stage + 1 == STAGES ? 0u : stage + 1;
-        phase = stage == 0 ? phase ^ 1u : phase;
+        sf_stage = sf_stage + 1 == L::SF_SMEM_STAGES ? 0u : sf_stage + 1;
+        sf_phase = sf_stage == 0 ? sf_phase ^ 1u : sf_phase;
       }
     }
   }
@@ -197,10 +214,10 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
 
 // ---------------------------------------------------------------- scale copiers (leader)
 // Copier c moves, for every stage, the scale blocks of MMA c (SFA, SFB rows 0-127, SFB
-// rows 128-255: 3 copies) from shared memory to the stage's TMEM scale slot, then commits
-// to sf_ready. Waiting for the stage's data also guarantees that the MMAs STAGES stages
-// earlier, which read the same TMEM slot, have completed: the producers could not reload
-// the stage before their commit.
+// rows 128-255: 3 copies) from the stage's shared-memory scale slot to its TMEM scale slot,
+// arrives on sf_ready, and commits the copies to sf_free (their completion frees the
+// shared-memory slot for the scale producer). Before writing the TMEM slot it waits for the
+// MMAs of the stage that used the slot last.
 template <int STAGES>
 __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx& x) {
   using L = Nvfp4Layout<STAGES>;
@@ -210,18 +227,33 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
   const uint64_t sfa0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFA, 128), c * L::SF_BLOCK);
   const uint64_t sfb0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFB, 128), c * L::SF_BLOCK);
   const uint32_t col0 = x.tmem_base + L::SF_TMEM_COL0;
-  uint32_t stage = 0, phase = 0;
+  uint32_t stage = 0, phase = 0;      // A/B ring: full and sf_ready barriers
+  uint32_t sf_smem = 0;               // scale ring in shared memory
+  uint32_t sf_stage = 0;              // scale ring in TMEM
+  uint32_t e_stage = 0, e_phase = 0;  // A/B ring position of stage g - SF_STAGES
   bool ok = true;
-  // straight-line loop body: the ring position advances by selects
+  // straight-line loop body: the ring positions advance by selects
 #pragma unroll 2
   for (long long g = 0; g < total; ++g) {
     if (!wait_phase_inline(x.bar_full + 8 * stage, phase, x.wctx, status_code(kRoleScales, 0x300 + stage))) {
       ok = false;
       break;
     }
-    const uint64_t sfa = umma_desc_advance(sfa0, stage * L::SFA_BYTES);
-    const uint64_t sfb = umma_desc_advance(sfb0, stage * L::SFB_BYTES);
-    const uint32_t col = col0 + stage * L::SF_COLS;
+    if constexpr (L::SF_STAGES < STAGES) {
+      // The TMEM slot's previous stage (g - SF_STAGES) must have completed its MMAs, which
+      // read the scales there. (With equal rings the producers' wait implies it.)
+      if (g >= L::SF_STAGES) {
+        if (!wait_phase_inline(x.bar_empty + 8 * e_stage, e_phase, x.wctx, status_code(kRoleScales, 0x400 + e_stage))) {
+          ok = false;
+          break;
+        }
+        e_stage = e_stage + 1 == STAGES ? 0u : e_stage + 1;
+        e_phase = e_stage == 0 ? e_phase ^ 1u : e_phase;
+      }
+    }
+    const uint64_t sfa = umma_desc_advance(sfa0, sf_smem * L::SFA_BYTES);
+    const uint64_t sfb = umma_desc_advance(sfb0, sf_smem * L::SFB_BYTES);
+    const uint32_t col = col0 + sf_stage * L::SF_COLS;
     tc_fence_after_sync();
     tmem_cp_32x128b_warpx4<2>(col + 4 * c, sfa);
     tmem_cp_32x128b_warpx4<2>(col + 16 + 8 * c, sfb);
@@ -232,8 +264,12 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
     // not wait for the copies to complete (a tcgen05.commit here would make it: -2.4%).
     tc_fence_before_sync();
     mbar_arrive_local(x.bar_sfready + 8 * stage);
+    // the scale slot's shared memory (in both CTAs) is free once these copies complete
+    mma_commit_pair_multicast(x.bar_sffree + 8 * sf_smem, 0x3);
     stage = stage + 1 == STAGES ? 0u : stage + 1;
     phase = stage == 0 ? phase ^ 1u : phase;
+    sf_smem = sf_smem + 1 == L::SF_SMEM_STAGES ? 0u : sf_smem + 1;
+    sf_stage = sf_stage + 1 == L::SF_STAGES ? 0u : sf_stage + 1;
   }
   if (!ok) settle_after_abort();
 }
@@ -243,11 +279,12 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
 // memory and TMEM scales). Descriptors and scale columns follow from the ring position.
 template <int STAGES>
 __device__ __forceinline__ void mma_stage(const Nvfp4Ctx& x, uint64_t a_desc0, uint64_t b_desc0, uint32_t sf_col0,
-                                          uint32_t idesc, uint32_t sfb_half_col, uint32_t stage, bool first) {
+                                          uint32_t idesc, uint32_t sfb_half_col, uint32_t stage, uint32_t sf_stage,
+                                          bool first) {
   using L = Nvfp4Layout<STAGES>;
   const uint64_t a_desc = umma_desc_advance(a_desc0, stage * L::A_BYTES);
   const uint64_t b_desc = umma_desc_advance(b_desc0, stage * L::B_BYTES);
-  const uint32_t sf_col = sf_col0 + stage * L::SF_COLS;
+  const uint32_t sf_col = sf_col0 + sf_stage * L::SF_COLS;
 #pragma unroll
   for (int j = 0; j < L::KSTEPS; ++j) {
     const uint32_t koff = j * (L::UMMA_K / 2);  // 32 bytes of packed codes per MMA
@@ -269,7 +306,8 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
   if (x.rank != 0 || x.lane != 0) return;
   constexpr uint32_t IDESC_FULL = idesc_nvf4(L::TILE_M, L::BLOCK_N);
   constexpr uint32_t IDESC_HALF = idesc_nvf4(L::TILE_M, L::BLOCK_N / 2);
-  uint32_t stage = 0, phase = 0;
+  uint32_t stage = 0, phase = 0;  // A/B ring
+  uint32_t sf_stage = 0;          // scale ring (TMEM slot)
   bool ok = true;
   if (p.debug_flags & 1u) ok = wait_phase_inline(x.bar_never, 0, x.wctx, status_code(kRoleMma, 0xFFFF));
   const uint64_t a_desc0 = umma_desc_sw128(x.base + L::OFF_A), b_desc0 = umma_desc_sw128(x.base + L::OFF_B);
@@ -290,24 +328,27 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
     for (int q = 0; q < pairs; ++q, kb += 2) {
       const uint32_t s1 = stage + 1 == STAGES ? 0u : stage + 1;
       const uint32_t ph1 = s1 == 0 ? phase ^ 1u : phase;
+      const uint32_t f1 = sf_stage + 1 == L::SF_STAGES ? 0u : sf_stage + 1;
       if (!wait_phase_inline(x.bar_sfready + 8 * s1, ph1, x.wctx, status_code(kRoleMma, 0x200 + s1))) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, kb == 0);
-      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, s1, false);
+      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, sf_stage, kb == 0);
+      mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, s1, f1, false);
       stage = s1 + 1 == STAGES ? 0u : s1 + 1;
       phase = stage == 0 ? ph1 ^ 1u : ph1;
+      sf_stage = f1 + 1 == L::SF_STAGES ? 0u : f1 + 1;
     }
     if (ok && kb < p.k_iters) {  // an odd number of stages: the last one alone
       if (!wait_phase_inline(x.bar_sfready + 8 * stage, phase, x.wctx, status_code(kRoleMma, 0x200 + stage))) {
         ok = false;
       } else {
         tc_fence_after_sync();
-        mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, kb == 0);
+        mma_stage<STAGES>(x, a_desc0, b_desc0, sf_col0, idesc, sfb_half_col, stage, sf_stage, kb == 0);
         stage = stage + 1 == STAGES ? 0u : stage + 1;
         phase = stage == 0 ? phase ^ 1u : phase;
+        sf_stage = sf_stage + 1 == L::SF_STAGES ? 0u : sf_stage + 1;
       }
     }
     if (!ok) break;
@@ -359,25 +400,21 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
     __syncwarp();
     if (lane == 0) mbar_arrive_cluster_relaxed(tempty_leader);  // orders tcgen05 work only
     if (live) {
+      // 16 columns at a time: lane r writes its row's 32 bytes to the 32 x 16 staging tile,
+      // one TMA store writes the tile (clipped at M and N)
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col = col0 + cc * 64;
+      for (int e = 0; e < 128 / L::EPI_COLS; ++e) {
+        const int col = col0 + e * L::EPI_COLS;
         if (col < p.N) {
-          uint32_t pk[32];
+          const uint32_t* s = &v[e >> 1][(e & 1) * 16];
+          uint32_t pk[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            pk[e] = pack_bf16x2_rn(v[2 * cc][2 * e], v[2 * cc][2 * e + 1]);
-            pk[16 + e] = pack_bf16x2_rn(v[2 * cc + 1][2 * e], v[2 * cc + 1][2 * e + 1]);
-          }
+          for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2_rn(s[2 * k], s[2 * k + 1]);
           if (lane == 0) bulk_wait_group_read<0>();  // the store that last read `buf` is done
           __syncwarp();
-          // row `lane` of the 32 x 64 staging tile, 16-byte chunk j at j ^ (row % 8):
-          // the C tensor map's 128-byte swizzle, bank-conflict free
-          const uint32_t row_addr = buf + lane * 128u;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
-                         pk[4 * j + 2], pk[4 * j + 3]);
+          const uint32_t row_addr = buf + lane * (L::EPI_COLS * 2);
+          st_shared_v4(row_addr, pk[0], pk[1], pk[2], pk[3]);
+          st_shared_v4(row_addr + 16, pk[4], pk[5], pk[6], pk[7]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -424,7 +461,8 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   x.bar_full = x.base + L::OFF_BAR;             // stage landed (leader's, bytes of both CTAs)
   x.bar_empty = x.bar_full + 8 * STAGES;        // stage consumed by the MMAs (both CTAs)
   x.bar_sfready = x.bar_empty + 8 * STAGES;     // stage's scales copied to TMEM (leader's)
-  x.bar_tfull = x.bar_sfready + 8 * STAGES;     // accumulator ready
+  x.bar_sffree = x.bar_sfready + 8 * STAGES;    // scale slot's copies done (both CTAs, 4 commits)
+  x.bar_tfull = x.bar_sffree + 8 * L::SF_SMEM_STAGES;  // accumulator ready
   x.bar_tempty = x.bar_tfull + 8;               // accumulator drained (leader's, 8 arrivals)
   x.bar_never = x.bar_tempty + 8;               // nobody arrives (timeout-path test)
   x.bar_drain = x.bar_never + 8;                // MMA drain after an abort
@@ -438,6 +476,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
       mbar_init(x.bar_empty + 8 * s, 1);
       mbar_init(x.bar_sfready + 8 * s, L::COPY_WARPS);
     }
+    for (int s = 0; s < L::SF_SMEM_STAGES; ++s) mbar_init(x.bar_sffree + 8 * s, L::COPY_WARPS);
     mbar_init(x.bar_tfull, 1);
     mbar_init(x.bar_tempty, L::EPI_WARPS * L::CG);
     mbar_init(x.bar_never, 1);
@@ -489,7 +528,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
 
 namespace {
 
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 using NL = Nvfp4Layout<kStages>;
 constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kStages>;
 
@@ -554,9 +593,9 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
     const uint32_t box[3] = {128, NL::KSTEPS, 2};
     st = encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, dims, strides, box);
   }
-  if (st == GEMM_OK)
-    st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+  if (st == GEMM_OK)  // C stores: 32 rows x 16 columns of BF16 per box
+    st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, NL::EPI_COLS, 32,
+                        CU_TENSOR_MAP_SWIZZLE_NONE);
   if (st != GEMM_OK) return st;
 
   Nvfp4Params p;
