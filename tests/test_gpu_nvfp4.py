@@ -119,12 +119,35 @@ def test_random_scales(shape, path):
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 2), (5, 1)])
-def test_many_tiles_per_cluster(max_clusters, group_m, path):
-    M, N, K = 1280, 1024, 1536    # 5 x 4 tiles, 6 K stages: the stage ring wraps inside a tile
+@pytest.mark.parametrize("max_clusters,group_m,K", [(1, 0, 1536), (3, 2, 1536), (5, 1, 1536), (1, 0, 1792), (3, 1, 2304)])
+def test_many_tiles_per_cluster(max_clusters, group_m, K, path):
+    # 5 x 4 tiles, 6, 7 or 9 K stages per tile: with tiles following one another on a cluster,
+    # the A/B ring (6 slots) and the two scale rings (4 and 5 slots) start each tile at
+    # different positions, and an odd stage count ends each tile with a single stage
+    M, N = 1280, 1024
     a, sfa, b, sfb = si.nvfp4_problem(21, M, N, K)
     assert_nvfp4_close(run(a, sfa, b, sfb, path, max_clusters=max_clusters, group_m=group_m),
-                       oracle.gemm_nvfp4(a, sfa, b, sfb), f"clusters {max_clusters}")
+                       oracle.gemm_nvfp4(a, sfa, b, sfb), f"clusters {max_clusters}, K {K}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_output_guard_band_untouched(path):
+    """Nothing outside the M x N output is written: the last 16-column store box of each row
+    block is half outside N (264 = 16 * 16 + 8) and the last row block is cut at M."""
+    M, N, K = 300, 264, 512
+    a, sfa, b, sfb = (t.to(DEV) for t in si.nvfp4_problem(23, M, N, K))
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), 12345.0, dtype=torch.bfloat16, device=DEV)
+    sentinel = bits(buf[:pad]).copy()
+    C = buf[pad:pad + M * N].view(M, N)
+    if path == "blocked_scales":
+        g.gemm_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb), C, M, N, K)
+    else:
+        g.gemm_nvfp4(a, sfa, b, sfb, C, M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(buf[:pad]), sentinel)
+    assert np.array_equal(bits(buf[pad + M * N:]), sentinel)
+    assert_nvfp4_close(bits(C), oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu()), "guard band")
 
 
 @pytest.mark.parametrize("path", PATHS)
