@@ -204,8 +204,38 @@ def set_bytes(cfg):
     return (M * K + N * K) // 2 + (M * K + N * K) // 16 + 2 * M * N
 
 
-def launch(g, cfg, ins, C, stream, opts, scales="blocked"):
+# Fused epilogues selectable with --epilogue: (alpha, beta, with bias, activation name).
+EPILOGUES = {
+    "none": None,
+    "relu_bias": (1.0, 0.0, True, "relu"),
+    "gelu_beta_bias": (0.5, 1.0, True, "gelu_tanh"),
+}
+
+
+def make_epilogue(g, name, N, device):
+    import torch
+    spec = EPILOGUES[name]
+    if spec is None:
+        return None
+    alpha, beta, with_bias, act = spec
+    gen = torch.Generator().manual_seed(7)
+    bias = torch.empty(N).uniform_(-1, 1, generator=gen).to(torch.bfloat16).to(device) if with_bias else None
+    code = {"relu": g.GEMM_ACT_RELU, "gelu_tanh": g.GEMM_ACT_GELU_TANH}[act]
+    ep = g.epilogue(alpha, beta, bias, code)
+    ep._bias_keepalive = bias
+    return ep
+
+
+def launch(g, cfg, ins, C, stream, opts, scales="blocked", epi=None):
     M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    if epi is not None:
+        if cfg["kind"] == "bf16":
+            g.gemm_bf16_fused(ins[0], ins[1], C, M, N, K, epi, stream, opts)
+        elif scales == "blocked":
+            g.gemm_nvfp4_blocked_fused(ins[0], ins[1], ins[2], ins[3], C, M, N, K, epi, stream, opts)
+        else:
+            g.gemm_nvfp4_fused(ins[0], ins[1], ins[2], ins[3], C, M, N, K, epi, stream, opts)
+        return
     if cfg["kind"] == "bf16":
         g.gemm_bf16(ins[0], ins[1], C, M, N, K, stream, opts)
     elif scales == "blocked":
@@ -335,8 +365,9 @@ def run_ours(args, cfg, world, rank, local):
     sb = set_bytes(cfg)
     R = max(3, math.ceil(2 * l2 / sb) + 1)
     sets = [make_inputs(cfg, r, dev, args.scales) for r in range(R)]
-    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    outs = [torch.zeros(M, N, dtype=torch.bfloat16, device=dev) for _ in range(R)]
     stream = torch.cuda.Stream(device=dev)
+    epi = make_epilogue(g, args.epilogue, N, dev)
     opts = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
                      persistent=0 if args.no_persistent else 1, no_tail_split=1 if args.no_tail_split else 0,
                      no_pdl=1 if args.no_pdl else 0)
@@ -345,7 +376,7 @@ def run_ours(args, cfg, world, rank, local):
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales)
+            launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
     stream.synchronize()
     st, detail = g.get_device_status(stream)
     if st != 0:
@@ -369,7 +400,7 @@ def run_ours(args, cfg, world, rank, local):
         clocks.mark_start()
     ev0.record(stream)
     for i in range(args.steps):
-        launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales)
+        launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
     ev1.record(stream)
     stream.synchronize()
     if clocks:
@@ -415,7 +446,7 @@ def run_ours(args, cfg, world, rank, local):
         stream.wait_event(ev_in[b])
         if used[b]:
             stream.wait_event(ev_out[b])      # the copy-out of step i-2 has read dev_out[b]
-        launch(g, cfg, dev_in[b], dev_out[b], stream, opts, args.scales)
+        launch(g, cfg, dev_in[b], dev_out[b], stream, opts, args.scales, epi)
         ev_gemm[b].record(stream)
         s_out.wait_event(ev_gemm[b])
         with torch.cuda.stream(s_out):
@@ -461,7 +492,9 @@ def run_ours(args, cfg, world, rank, local):
             rate.update({"ceiling_at_sampled_clock": ceiling, "frac_of_ceiling": achieved / ceiling})
     except Exception as e:  # report, do not fail the benchmark line
         rate = {"error": str(e)}
-    traffic = recorded_traffic(cfg["workload"] + ("" if cfg["kind"] == "bf16" else f"_{args.scales}"), cfg["kind"])
+    # the recorded counters are those of the plain kernel
+    traffic = (recorded_traffic(cfg["workload"] + ("" if cfg["kind"] == "bf16" else f"_{args.scales}"), cfg["kind"])
+               if args.epilogue == "none" else None)
     cpu = cpu_baseline(cfg, args.cpu_seconds) if not args.no_cpu_baseline else None
     if cpu:
         cpu.pop("seconds", None)
@@ -492,6 +525,10 @@ def run_ours(args, cfg, world, rank, local):
                        "blocked tensor-core layout (packed once at input setup)" if args.scales == "blocked"
                        else "row-major [rows][K/16], packed to the tensor-core layout inside each call"),
             "group_m": args.group_m or "auto",
+            "epilogue": ("plain BF16 rounding" if args.epilogue == "none" else
+                         f"fused {args.epilogue}: alpha, beta, bias, activation = {EPILOGUES[args.epilogue]}"
+                         + (" (e2e: the prior C is the device buffer's previous contents)"
+                            if EPILOGUES[args.epilogue][1] != 0.0 else "")),
             "baseline": "HGEMM v7 on GB300, 1980.925 TFLOP/s (page 1 Performance table)" if baseline else None,
         },
         "roofline": {
@@ -530,6 +567,8 @@ def main():
     ap.add_argument("--no-persistent", action="store_true")
     ap.add_argument("--no-tail-split", action="store_true")
     ap.add_argument("--scales", default="blocked", choices=["blocked", "rowmajor"])
+    ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
+                    help="fused epilogue of the *_fused calls (default: the plain GEMM)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -40,8 +40,13 @@ EXPORTS = (
     "gemm_bf16", "gemm_nvfp4", "gemm_status_string", "gemm_get_device_status", "gemm_bf16_ex",
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
-    "gemm_nvfp4_noalloc", "gemm_measure_mma_rate",
+    "gemm_nvfp4_noalloc", "gemm_measure_mma_rate", "gemm_bf16_fused", "gemm_nvfp4_fused", "gemm_nvfp4_blocked_fused",
 )
+
+# gemm_activation_t
+GEMM_ACT_NONE = 0
+GEMM_ACT_RELU = 1
+GEMM_ACT_GELU_TANH = 2
 
 
 class GemmError(RuntimeError):
@@ -67,6 +72,21 @@ class gemm_options_t(ctypes.Structure):
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
             no_tail_split=0, no_pdl=0):
     return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl)
+
+
+class gemm_epilogue_t(ctypes.Structure):
+    _fields_ = [
+        ("alpha", ctypes.c_float),
+        ("beta", ctypes.c_float),
+        ("bias", ctypes.c_void_p),
+        ("activation", ctypes.c_int),
+        ("reserved", ctypes.c_int),
+    ]
+
+
+def epilogue(alpha=1.0, beta=0.0, bias=None, activation=GEMM_ACT_NONE) -> gemm_epilogue_t:
+    """C = act(alpha * A B^T + beta * C + bias[col]); `bias` is a device tensor of N BF16 values or None."""
+    return gemm_epilogue_t(alpha, beta, None if bias is None else _ptr(bias), activation, 0)
 
 
 _lib = None
@@ -111,6 +131,13 @@ def lib() -> ctypes.CDLL:
         l.gemm_launch_count.argtypes = []
         l.gemm_launch_count.restype = ctypes.c_ulonglong
         l.gemm_measure_mma_rate.argtypes = [I, ctypes.POINTER(ctypes.c_double)]
+        EP, OP = ctypes.POINTER(gemm_epilogue_t), ctypes.POINTER(gemm_options_t)
+        l.gemm_bf16_fused.argtypes = [P, P, P, I, I, I, P, EP, OP]
+        l.gemm_bf16_fused.restype = I
+        l.gemm_nvfp4_fused.argtypes = [P, P, P, P, P, I, I, I, P, EP, OP]
+        l.gemm_nvfp4_fused.restype = I
+        l.gemm_nvfp4_blocked_fused.argtypes = [P, P, P, P, P, I, I, I, P, EP, OP]
+        l.gemm_nvfp4_blocked_fused.restype = I
         l.gemm_measure_mma_rate.restype = I
         _lib = l
     return _lib
@@ -190,6 +217,33 @@ def gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M: int, N: int, K: int
         st = l.gemm_nvfp4_blocked_ex(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
                                      _stream(stream), ctypes.byref(opts))
     _check(st, "gemm_nvfp4_blocked")
+
+
+def _byref_or_null(x):
+    return None if x is None else ctypes.byref(x)
+
+
+def gemm_bf16_fused(A, B, C, M: int, N: int, K: int, epi: gemm_epilogue_t | None = None, stream=None,
+                    opts: gemm_options_t | None = None) -> None:
+    """gemm_bf16 with the fused epilogue C = act(alpha * A B^T + beta * C + bias)."""
+    _check(lib().gemm_bf16_fused(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream), _byref_or_null(epi),
+                                 _byref_or_null(opts)), "gemm_bf16_fused")
+
+
+def gemm_nvfp4_fused(A, SFA, B, SFB, C, M: int, N: int, K: int, epi: gemm_epilogue_t | None = None, stream=None,
+                     opts: gemm_options_t | None = None) -> None:
+    """gemm_nvfp4 with the fused epilogue."""
+    _check(lib().gemm_nvfp4_fused(_ptr(A), _ptr(SFA), _ptr(B), _ptr(SFB), _ptr(C), M, N, K, _stream(stream),
+                                  _byref_or_null(epi), _byref_or_null(opts)), "gemm_nvfp4_fused")
+
+
+def gemm_nvfp4_blocked_fused(A, SFA_blocked, B, SFB_blocked, C, M: int, N: int, K: int,
+                             epi: gemm_epilogue_t | None = None, stream=None,
+                             opts: gemm_options_t | None = None) -> None:
+    """gemm_nvfp4_blocked with the fused epilogue."""
+    _check(lib().gemm_nvfp4_blocked_fused(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
+                                          _stream(stream), _byref_or_null(epi), _byref_or_null(opts)),
+           "gemm_nvfp4_blocked_fused")
 
 
 def gemm_nvfp4_noalloc(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None) -> None:

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "common.cuh"
 #include "gemm.h"
 #include "host_common.h"
 #include "schedule.h"
@@ -225,16 +226,62 @@ static int zero_output(void* C, int M, int N, cudaStream_t stream) {
   return GEMM_OK;
 }
 
+// Checks a gemm_epilogue_t; NULL is the identity.
+static int resolve_epilogue(const gemm_epilogue_t* e, EpilogueOptions* r) {
+  if (e == nullptr) return GEMM_OK;
+  if (e->reserved != 0) return GEMM_ERR_INVALID_ARG;
+  if (e->activation != GEMM_ACT_NONE && e->activation != GEMM_ACT_RELU && e->activation != GEMM_ACT_GELU_TANH)
+    return GEMM_ERR_INVALID_ARG;
+  if (e->bias != nullptr && !aligned16(e->bias)) return GEMM_ERR_MISALIGNED;
+  r->alpha = e->alpha;
+  r->beta = e->beta;
+  r->bias = e->bias;
+  r->act = e->activation;
+  return GEMM_OK;
+}
+
+// K == 0 with a fused epilogue: the product is zero, so C = act(beta * C + bias), 8
+// elements (one 16-byte vector; N is a multiple of 8) per thread and step.
+__global__ void epilogue_only_kernel(uint16_t* C, long long vectors, int N, EpiParams e) {
+  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < vectors;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    uint4* c = reinterpret_cast<uint4*>(C) + v;
+    const int col = static_cast<int>((v * 8) % N);
+    const uint4 old = e.beta != 0.0f ? *c : make_uint4(0u, 0u, 0u, 0u);  // beta == 0: C is not read
+    const uint4 b = epi_bias8(e, col, N);
+    *c = make_uint4(epi_pair(0u, 0u, old.x, b.x, e), epi_pair(0u, 0u, old.y, b.y, e), epi_pair(0u, 0u, old.z, b.z, e),
+                    epi_pair(0u, 0u, old.w, b.w, e));
+  }
+}
+
+static int empty_sum_output(void* C, int M, int N, cudaStream_t stream, const EpilogueOptions& epi, int num_sms) {
+  if (!epi.fused()) return zero_output(C, M, N, stream);
+  EpiParams e;
+  e.alpha = epi.alpha;
+  e.beta = epi.beta;
+  e.bias = static_cast<const uint16_t*>(epi.bias);
+  e.act = epi.act;
+  e.fused = 1;
+  const long long vectors = static_cast<long long>(M) * N / 8;
+  const long long want = (vectors + 255) / 256;
+  const int blocks = static_cast<int>(std::min<long long>(want, 8LL * std::max(num_sms, 1)));
+  epilogue_only_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint16_t*>(C), vectors, N, e);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  count_launch();
+  return GEMM_OK;
+}
+
 }  // namespace dtcp
 
 using namespace dtcp;
 
 extern "C" {
 
-int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
-                 const gemm_options_t* options) {
+int gemm_bf16_fused(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
+                    const gemm_epilogue_t* epilogue, const gemm_options_t* options) {
   RunOptions opt;
   int st = resolve_options(options, &opt);
+  if (st == GEMM_OK) st = resolve_epilogue(epilogue, &opt.epi);
   if (st != GEMM_OK) return st;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return GEMM_OK;
@@ -242,20 +289,27 @@ int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, voi
   if (K % 8 != 0 || N % 8 != 0) return GEMM_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return GEMM_ERR_MISALIGNED;
   int device = 0, err = 0;
-  if (current_device_info(&device, &err) == nullptr) return err;
+  const DeviceInfo* info = current_device_info(&device, &err);
+  if (info == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(C, M, N, s);
+  if (K == 0) return empty_sum_output(C, M, N, s, opt.epi, info->num_sms);
   return run_gemm_bf16(A, B, C, M, N, K, s, opt);
+}
+
+int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
+                 const gemm_options_t* options) {
+  return gemm_bf16_fused(A, B, C, M, N, K, stream, nullptr, options);
 }
 
 int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* stream) {
   return gemm_bf16_ex(A, B, C, M, N, K, stream, nullptr);
 }
 
-int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
-                  void* stream, const gemm_options_t* options) {
+int gemm_nvfp4_fused(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                     void* stream, const gemm_epilogue_t* epilogue, const gemm_options_t* options) {
   RunOptions opt;
   int st = resolve_options(options, &opt);
+  if (st == GEMM_OK) st = resolve_epilogue(epilogue, &opt.epi);
   if (st != GEMM_OK) return st;
   if (opt.kernel != GEMM_KERNEL_DEFAULT) return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
@@ -267,9 +321,10 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   if (!aligned16(C) || (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA) || !aligned16(SFB))))
     return GEMM_ERR_MISALIGNED;
   int device = 0, err = 0;
-  if (current_device_info(&device, &err) == nullptr) return err;
+  const DeviceInfo* info = current_device_info(&device, &err);
+  if (info == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(C, M, N, s);
+  if (K == 0) return empty_sum_output(C, M, N, s, opt.epi, info->num_sms);
   // Rearrange both scale matrices into the blocked layout in a stream-ordered workspace,
   // run the blocked GEMM, and free the workspace in stream order behind it.
   const size_t bytes_a = round_up(static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(M, K)), 256);
@@ -286,6 +341,11 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, sfa_blk, B, sfb_blk, C, M, N, K, s, opt);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;
+}
+
+int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                  void* stream, const gemm_options_t* options) {
+  return gemm_nvfp4_fused(A, SFA, B, SFB, C, M, N, K, stream, nullptr, options);
 }
 
 int gemm_nvfp4(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
@@ -309,10 +369,12 @@ int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, vo
   return run_pack_scales(SF, SF_blocked, rows, K, static_cast<cudaStream_t>(stream));
 }
 
-int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
-                          int M, int N, int K, void* stream, const gemm_options_t* options) {
+int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                             int M, int N, int K, void* stream, const gemm_epilogue_t* epilogue,
+                             const gemm_options_t* options) {
   RunOptions opt;
   int st = resolve_options(options, &opt);
+  if (st == GEMM_OK) st = resolve_epilogue(epilogue, &opt.epi);
   if (st != GEMM_OK) return st;
   if (opt.kernel != GEMM_KERNEL_DEFAULT) return GEMM_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
@@ -324,10 +386,16 @@ int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B,
       (K > 0 && (!aligned16(A) || !aligned16(B) || !aligned16(SFA_blocked) || !aligned16(SFB_blocked))))
     return GEMM_ERR_MISALIGNED;
   int device = 0, err = 0;
-  if (current_device_info(&device, &err) == nullptr) return err;
+  const DeviceInfo* info = current_device_info(&device, &err);
+  if (info == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (K == 0) return zero_output(C, M, N, s);
+  if (K == 0) return empty_sum_output(C, M, N, s, opt.epi, info->num_sms);
   return run_gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt);
+}
+
+int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                          int M, int N, int K, void* stream, const gemm_options_t* options) {
+  return gemm_nvfp4_blocked_fused(A, SFA_blocked, B, SFB_blocked, C, M, N, K, stream, nullptr, options);
 }
 
 int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C, int M,

@@ -126,4 +126,50 @@ __device__ __forceinline__ void settle_after_abort() {
   while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
 }
 
+// ---------------------------------------------------------------- fused epilogue
+
+// C = act(alpha * acc + beta * C_old + bias[col]), in FP32, rounded once to BF16.
+// `fused` is 0 for the plain epilogue (alpha 1, beta 0, no bias, no activation).
+struct EpiParams {
+  float alpha, beta;
+  const uint16_t* bias;  // N BF16 values, or null
+  int act;               // 0 none, 1 ReLU, 2 GELU (tanh form)
+  int fused;
+};
+
+__device__ __forceinline__ float epi_activation(float x, int act) {
+  if (act == 1) return fmaxf(x, 0.0f);
+  if (act == 2) {
+    // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as
+    // x / (1 + exp(-2u)) (the same function: 0.5 (1 + tanh u) is the logistic function of
+    // 2u), with the exponential intrinsic: a few instructions instead of a tanh expansion.
+    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
+    float r;  // 1 / (1 + exp(-2u)); rcp.approx of +inf (exp overflow) is 0, so x * r = -0
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-2.0f * u)));
+    return x * r;
+  }
+  return x;
+}
+
+// One pair of adjacent columns: FP32 accumulator bits acc0 / acc1, the prior C and the
+// bias as BF16 pairs (element 0 in the low half).
+__device__ __forceinline__ uint32_t epi_pair(uint32_t acc0, uint32_t acc1, uint32_t old2, uint32_t bias2,
+                                             const EpiParams& e) {
+  float x0 = e.alpha * __uint_as_float(acc0), x1 = e.alpha * __uint_as_float(acc1);
+  if (e.beta != 0.0f) {
+    x0 = fmaf(e.beta, __uint_as_float(old2 << 16), x0);
+    x1 = fmaf(e.beta, __uint_as_float(old2 & 0xFFFF0000u), x1);
+  }
+  x0 += __uint_as_float(bias2 << 16);
+  x1 += __uint_as_float(bias2 & 0xFFFF0000u);
+  return pack_bf16x2_rn(__float_as_uint(epi_activation(x0, e.act)), __float_as_uint(epi_activation(x1, e.act)));
+}
+
+// Bias of 8 consecutive columns starting at `col` (a multiple of 8) as 4 BF16 pairs; zero
+// past N (N is a multiple of 8) or without a bias.
+__device__ __forceinline__ uint4 epi_bias8(const EpiParams& e, int col, int N) {
+  if (e.bias == nullptr || col >= N) return make_uint4(0u, 0u, 0u, 0u);
+  return __ldg(reinterpret_cast<const uint4*>(e.bias + col));
+}
+
 }  // namespace dtcp

@@ -45,6 +45,7 @@ struct Bf16Params {
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
   int zigzag;  // 1: a cluster's odd-numbered tiles walk K downwards
+  EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
 };
 
 template <int CG, int STAGES, int ATOMS>
@@ -74,8 +75,8 @@ struct Bf16Layout {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2;
+  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain, c_loaded[EPI_WARPS]
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 + EPI_WARPS;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
   const uint32_t bar_tempty = bar_tfull + 16;        // tmem_empty[slot]: accumulator drained
   const uint32_t bar_never = bar_tempty + 16;        // nobody arrives (timeout-path test)
   const uint32_t bar_drain = bar_never + 8;          // MMA drain after an abort
+  const uint32_t bar_cload = bar_drain + 8;          // c_loaded[w]: epilogue warp w's prior-C tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   const WaitCtx wctx{abort_flag, p.status, p.wait_limit_ns};
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
     }
     mbar_init(bar_never, 1);
     mbar_init(bar_drain, 1);
+    for (int w = 0; w < L::EPI_WARPS; ++w) mbar_init(bar_cload + 8 * w, 1);
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
     prefetch_tensormap(&tmap_a);
@@ -287,6 +290,9 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
     const uint32_t epi = warp - 2u;
     const uint32_t stage_base = base + L::OFF_EPI + epi * L::EPI_BUFS * L::EPI_BUF_BYTES;
     const uint32_t tempty_target = (CG == 2) ? mapa_shared(bar_tempty, 0) : bar_tempty;
+    const uint32_t cload = bar_cload + 8 * epi;
+    uint32_t cload_phase = 0;
+    bool epi_ok = true;
     uint32_t ebuf = 0;
     int it = 0;
     for (int i = cluster_idx; i < p.num_items; i += num_clusters, ++it) {
@@ -295,10 +301,15 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
       const int chunks = (w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N) / 64;
       const uint32_t slot = static_cast<uint32_t>(it) & 1u;
       const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
-      if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
-      tc_fence_after_sync();
       const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M + static_cast<int>(q) * 32;
       const int col0 = tc.n_blk * L::BLOCK_N + (w.half > 0 ? L::BLOCK_N / 2 : 0);
+      if (p.epi.fused && p.epi.beta != 0.0f && lane == 0 && row0 < p.M) {
+        // the prior C of this warp's part of the tile into L2 while the MMAs still run
+        for (int c = 0; c < chunks; ++c)
+          if (col0 + c * 64 < p.N) tma_prefetch_l2_2d(&tmap_c, col0 + c * 64, row0);
+      }
+      if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
+      tc_fence_after_sync();
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * L::ACC_COLS;
       if (row0 < p.M) {
 #pragma unroll 1
@@ -309,18 +320,55 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           tmem_ld_32x32b_x32(taddr + c * 64, lo);
           tmem_ld_32x32b_x32(taddr + c * 64 + 32, hi);
           tmem_ld_wait();
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            pk[i] = pack_bf16x2_rn(lo[2 * i], lo[2 * i + 1]);
-            pk[16 + i] = pack_bf16x2_rn(hi[2 * i], hi[2 * i + 1]);
-          }
           const uint32_t buf = stage_base + ebuf * L::EPI_BUF_BYTES;
           if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
           __syncwarp();
           // Row `lane` of the 32 x 64 staging tile, 16-byte chunk j at position j ^ (row % 8):
           // the 128-byte swizzle the C tensor map uses (and bank-conflict free).
           const uint32_t row_addr = buf + lane * 128u;
+          uint32_t pk[32];
+          if (!p.epi.fused) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              pk[i] = pack_bf16x2_rn(lo[2 * i], lo[2 * i + 1]);
+              pk[16 + i] = pack_bf16x2_rn(hi[2 * i], hi[2 * i + 1]);
+            }
+          } else {
+            // prior C of the chunk (beta != 0): the 32 x 64 tile by TMA into the staging
+            // buffer (zeros past M and N), then row `lane` from it
+            uint32_t old[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) old[i] = 0u;
+            if (p.epi.beta != 0.0f) {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(cload, L::EPI_BUF_BYTES);
+                tma_load_2d(buf, &tmap_c, col, row0, cload);
+              }
+              if (!wait_phase_warp(cload, cload_phase, wctx, status_code(kRoleEpilogue, 2))) {
+                epi_ok = false;
+                break;
+              }
+              cload_phase ^= 1u;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                ld_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), old[4 * j], old[4 * j + 1],
+                             old[4 * j + 2], old[4 * j + 3]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint4 bb = epi_bias8(p.epi, col + 8 * j, p.N);
+              const uint32_t b4[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+              for (int t = 0; t < 4; ++t) {
+                const int e = 4 * j + t;  // pair index: columns 2e, 2e + 1 of the chunk
+                const uint32_t a0 = e < 16 ? lo[2 * e] : hi[2 * e - 32];
+                const uint32_t a1 = e < 16 ? lo[2 * e + 1] : hi[2 * e - 31];
+                pk[e] = epi_pair(a0, a1, old[e], b4[t], p.epi);
+              }
+            }
+            // every lane has read its row of the prior C before any lane overwrites it
+            __syncwarp();
+          }
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
@@ -334,6 +382,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           ebuf ^= 1u;
         }
       }
+      if (!epi_ok) break;  // a prior-C load timed out (status recorded)
       // Accumulator slot drained: hand it back to the MMA issuer (leader CTA's barrier).
       tmem_ld_wait();
       tc_fence_before_sync();
@@ -423,6 +472,11 @@ struct Bf16Variant {
     p.wait_limit_ns = opt.wait_limit_ns;
     p.debug_flags = opt.debug_flags;
     p.zigzag = 1;
+    p.epi.alpha = opt.epi.alpha;
+    p.epi.beta = opt.epi.beta;
+    p.epi.bias = static_cast<const uint16_t*>(opt.epi.bias);
+    p.epi.act = opt.epi.act;
+    p.epi.fused = opt.epi.fused() ? 1 : 0;
     if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
     const int max_clusters = max_active_clusters(device);

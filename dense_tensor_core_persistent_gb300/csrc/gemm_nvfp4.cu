@@ -62,6 +62,7 @@ struct Nvfp4Params {
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
   int zigzag;     // 1: a cluster's odd-numbered tiles walk K downwards
+  EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
 };
 
 template <int STAGES>
@@ -108,8 +109,9 @@ struct Nvfp4Layout {
   static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF_BYTES;
   // full[S], empty[S], sf_ready[S], tmem_full, tmem_empty, never, drain
-  // full[S], empty[S], sf_ready[S], sf_free[SF_SMEM_STAGES], tmem_full, tmem_empty, never, drain
-  static constexpr int NUM_BARS = 3 * STAGES + SF_SMEM_STAGES + 4;
+  // full[S], empty[S], sf_ready[S], sf_free[SF_SMEM_STAGES], tmem_full, tmem_empty, never, drain,
+  // c_loaded[EPI_WARPS]
+  static constexpr int NUM_BARS = 3 * STAGES + SF_SMEM_STAGES + 4 + EPI_WARPS;
   static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
@@ -131,7 +133,7 @@ struct Nvfp4Ctx {
   uint32_t warp, lane, rank;
   int cluster_idx, num_clusters, my_items;
   uint32_t tmem_base;
-  uint32_t bar_full, bar_empty, bar_sfready, bar_sffree, bar_tfull, bar_tempty, bar_never, bar_drain;
+  uint32_t bar_full, bar_empty, bar_sfready, bar_sffree, bar_tfull, bar_tempty, bar_never, bar_drain, bar_cload;
   WaitCtx wctx;
 };
 
@@ -364,7 +366,9 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
 }
 
 // ---------------------------------------------------------------- epilogue (warps 4..11)
-template <int STAGES>
+// FUSED: the epilogue of the *_fused calls (its own kernel instantiation, so that the
+// plain kernel's code stays as small as before).
+template <int STAGES, bool FUSED>
 __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtensorMap* tmap_c, const Nvfp4Ctx& x) {
   using L = Nvfp4Layout<STAGES>;
   const uint32_t lane = x.lane;
@@ -373,8 +377,11 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
   const int h = static_cast<int>(epi >> 2);        // accumulator columns 128h .. 128h+127
   const uint32_t buf = x.base + L::OFF_EPI + epi * L::EPI_BUF_BYTES;
   const uint32_t tempty_leader = mapa_shared(x.bar_tempty, 0);
+  const uint32_t cload = x.bar_cload + 8 * epi;
+  uint32_t cload_phase = 0;
+  bool epi_ok = true;
   int it = 0;
-  for (int i = x.cluster_idx; i < p.num_items; i += x.num_clusters, ++it) {
+  for (int i = x.cluster_idx; i < p.num_items && epi_ok; i += x.num_clusters, ++it) {
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
     const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
     const int width = w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N;  // accumulator columns of the item
@@ -383,6 +390,14 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
     // The tile coordinates (integer divisions) are computed while the MMAs run, not after
     // the wait below, where they would delay the release of TMEM by ~450 cycles.
     asm volatile("" : "+r"(row0), "+r"(col0));
+    if constexpr (FUSED) {
+      // the prior C of this warp's part of the tile into L2 while the MMAs still run
+      if (p.epi.beta != 0.0f && lane == 0 && row0 < p.M && h * 128 < width) {
+#pragma unroll 1
+        for (int e = 0; e < 128 / L::EPI_COLS; ++e)
+          if (col0 + e * L::EPI_COLS < p.N) tma_prefetch_l2_2d(tmap_c, col0 + e * L::EPI_COLS, row0);
+      }
+    }
     if (__all_sync(0xffffffffu, wait_phase_inline(x.bar_tfull, static_cast<uint32_t>(it) & 1u, x.wctx,
                                                    status_code(kRoleEpilogue, 0))) == 0)
       break;
@@ -407,12 +422,37 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
         const int col = col0 + e * L::EPI_COLS;
         if (col < p.N) {
           const uint32_t* s = &v[e >> 1][(e & 1) * 16];
-          uint32_t pk[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2_rn(s[2 * k], s[2 * k + 1]);
           if (lane == 0) bulk_wait_group_read<0>();  // the store that last read `buf` is done
           __syncwarp();
           const uint32_t row_addr = buf + lane * (L::EPI_COLS * 2);
+          uint32_t pk[8];
+          if constexpr (!FUSED) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2_rn(s[2 * k], s[2 * k + 1]);
+          } else {
+            // prior C (beta != 0): the 32 x 16 tile by TMA into the staging buffer (zeros
+            // past M and N), then row `lane` from it
+            uint32_t old[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            if (p.epi.beta != 0.0f) {
+              if (lane == 0) {
+                mbar_arrive_expect_tx(cload, L::EPI_BUF_BYTES);
+                tma_load_2d(buf, tmap_c, col, row0, cload);
+              }
+              if (__all_sync(0xffffffffu, wait_phase_inline(cload, cload_phase, x.wctx,
+                                                            status_code(kRoleEpilogue, 2))) == 0) {
+                epi_ok = false;
+                break;
+              }
+              cload_phase ^= 1u;
+              ld_shared_v4(row_addr, old[0], old[1], old[2], old[3]);
+              ld_shared_v4(row_addr + 16, old[4], old[5], old[6], old[7]);
+            }
+            const uint4 b0 = epi_bias8(p.epi, col, p.N), b1 = epi_bias8(p.epi, col + 8, p.N);
+            const uint32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pk[k] = epi_pair(s[2 * k], s[2 * k + 1], old[k], bb[k], p.epi);
+            __syncwarp();  // every lane has read its row of the prior C before any lane overwrites it
+          }
           st_shared_v4(row_addr, pk[0], pk[1], pk[2], pk[3]);
           st_shared_v4(row_addr + 16, pk[4], pk[5], pk[6], pk[7]);
           fence_proxy_async_smem();
@@ -440,7 +480,7 @@ __device__ __forceinline__ void teardown(const Nvfp4Ctx& x) {
   }
 }
 
-template <int STAGES>
+template <int STAGES, bool FUSED>
 __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_sfa,
@@ -466,6 +506,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   x.bar_tempty = x.bar_tfull + 8;               // accumulator drained (leader's, 8 arrivals)
   x.bar_never = x.bar_tempty + 8;               // nobody arrives (timeout-path test)
   x.bar_drain = x.bar_never + 8;                // MMA drain after an abort
+  x.bar_cload = x.bar_drain + 8;                // c_loaded[w]: epilogue warp w's prior-C tile landed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   x.wctx = WaitCtx{abort_flag, p.status, p.wait_limit_ns};
@@ -481,6 +522,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     mbar_init(x.bar_tempty, L::EPI_WARPS * L::CG);
     mbar_init(x.bar_never, 1);
     mbar_init(x.bar_drain, 1);
+    for (int w = 0; w < L::EPI_WARPS; ++w) mbar_init(x.bar_cload + 8 * w, 1);
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
     prefetch_tensormap(&tmap_a);
@@ -514,7 +556,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     teardown<STAGES>(x);
   } else if (x.warp < L::COPY_WARP0) {
     regs_increase<L::REGS_EPI>();
-    epilogue_role<STAGES>(p, &tmap_c, x);
+    epilogue_role<STAGES, FUSED>(p, &tmap_c, x);
     teardown<STAGES>(x);
   } else {
     regs_decrease<L::REGS_LOW>();
@@ -530,7 +572,8 @@ namespace {
 
 constexpr int kStages = 6;
 using NL = Nvfp4Layout<kStages>;
-constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kStages>;
+constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kStages, false>;
+constexpr auto kNvfp4KernelFused = nvfp4_gemm_kernel<kStages, true>;
 
 int max_active_clusters(int device) {
   static std::mutex mu;
@@ -538,7 +581,9 @@ int max_active_clusters(int device) {
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
   if (cache[device] > 0) return cache[device];
-  if (cudaFuncSetAttribute(kNvfp4Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) != cudaSuccess)
+  if (cudaFuncSetAttribute(kNvfp4Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) != cudaSuccess ||
+      cudaFuncSetAttribute(kNvfp4KernelFused, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) !=
+          cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -612,6 +657,11 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.wait_limit_ns = opt.wait_limit_ns;
   p.debug_flags = opt.debug_flags;
   p.zigzag = 1;
+  p.epi.alpha = opt.epi.alpha;
+  p.epi.beta = opt.epi.beta;
+  p.epi.bias = static_cast<const uint16_t*>(opt.epi.bias);
+  p.epi.act = opt.epi.act;
+  p.epi.fused = opt.epi.fused() ? 1 : 0;
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = max_active_clusters(device);
@@ -645,7 +695,8 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   attr[1].val.programmaticStreamSerializationAllowed = opt.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kNvfp4Kernel, ta, tb, tbh, tsa, tsb, tc, p);
+  const auto kernel = p.epi.fused ? kNvfp4KernelFused : kNvfp4Kernel;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tsa, tsb, tc, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;

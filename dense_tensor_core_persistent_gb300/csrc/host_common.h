@@ -37,6 +37,15 @@ unsigned* device_status_word(int device);
 void count_launch();
 
 // Resolved per-call options.
+// Fused epilogue of the *_fused calls: C = act(alpha * acc + beta * C_old + bias[col]).
+struct EpilogueOptions {
+  float alpha = 1.0f;
+  float beta = 0.0f;
+  const void* bias = nullptr;  // N BF16 values, or null
+  int act = 0;                 // 0 none, 1 ReLU, 2 GELU (tanh form)
+  bool fused() const { return alpha != 1.0f || beta != 0.0f || bias != nullptr || act != 0; }
+};
+
 struct RunOptions {
   int kernel = GEMM_KERNEL_DEFAULT;
   int persistent = 1;
@@ -46,6 +55,7 @@ struct RunOptions {
   int pdl = 1;  // programmatic stream serialization on the launch
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
+  EpilogueOptions epi;
 };
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,

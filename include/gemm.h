@@ -3,7 +3,8 @@
  *
  * Both GEMMs compute C = A * B^T on one GPU:
  *   A is M x K, B is N x K, both row-major with K contiguous ("K-major");
- *   C is M x N, row-major BF16, overwritten (no alpha/beta, no accumulate-into-C);
+ *   C is M x N, row-major BF16, overwritten (the *_fused calls add alpha/beta scaling,
+ *   a bias and an activation in the epilogue);
  *   products are accumulated in FP32 in tensor memory and rounded to BF16
  *   (round to nearest, ties to even) once, in the epilogue.
  *
@@ -220,6 +221,48 @@ int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB
 /* gemm_nvfp4_blocked with explicit options (as for gemm_nvfp4_ex). */
 int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                           int M, int N, int K, void* stream, const gemm_options_t* options);
+
+/*
+ * Fused epilogue ("NVFP4 GEMM on Blackwell", epilogue section: the accumulator in
+ * registers is where activation, bias and alpha/beta scaling belong). Each output element,
+ * while its FP32 accumulator is in registers:
+ *
+ *     C[i][j] = act(alpha * (A B^T)[i][j] + beta * C_old[i][j] + bias[j])
+ *
+ * evaluated in FP32 in that order and rounded once to BF16 (round to nearest, ties to
+ * even). act is the identity, max(x, 0), or the tanh form of GELU,
+ * 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+ *   alpha       scales the product.
+ *   beta        scales the prior contents of C. With beta == 0, C is not read (it may
+ *               hold anything, NaN included).
+ *   bias        device pointer to N BF16 values (one per column), 16-byte aligned, or NULL
+ *               for none. Caller-owned, read only.
+ *   activation  GEMM_ACT_NONE, GEMM_ACT_RELU or GEMM_ACT_GELU_TANH; anything else is
+ *               GEMM_ERR_INVALID_ARG.
+ *   reserved    must be 0.
+ * A NULL epilogue pointer is the identity (alpha 1, beta 0, no bias, no activation).
+ * With K == 0 the product is zero and the epilogue still applies to C.
+ */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU_TANH = 2 } gemm_activation_t;
+
+typedef struct {
+    float alpha;
+    float beta;
+    const void* bias;
+    int activation;
+    int reserved;
+} gemm_epilogue_t;
+
+/* gemm_bf16_ex, gemm_nvfp4_ex and gemm_nvfp4_blocked_ex with a fused epilogue. The
+ * arguments, layouts, preconditions and errors are those of the unfused calls, plus: a
+ * non-NULL bias not 16-byte aligned is GEMM_ERR_MISALIGNED. */
+int gemm_bf16_fused(const void* A, const void* B, void* C, int M, int N, int K, void* stream,
+                    const gemm_epilogue_t* epilogue, const gemm_options_t* options);
+int gemm_nvfp4_fused(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N, int K,
+                     void* stream, const gemm_epilogue_t* epilogue, const gemm_options_t* options);
+int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
+                             int M, int N, int K, void* stream, const gemm_epilogue_t* epilogue,
+                             const gemm_options_t* options);
 
 /*
  * gemm_tile_coord -- host evaluation of the persistent tile order used by the

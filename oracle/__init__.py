@@ -189,3 +189,40 @@ def ulp_bf16(r_bits: np.ndarray) -> np.ndarray:
 def bf16_bits_to_f64(bits) -> np.ndarray:
     b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- fused epilogue
+# "NVFP4 GEMM on Blackwell", epilogue section: activation, bias and alpha/beta scaling are
+# applied to the accumulator before it is stored. Reading taken here (the page names the
+# operations, not their order): x = alpha * acc + beta * C_old + bias[col], then the
+# activation, then one rounding to BF16.
+
+ACT_NONE, ACT_RELU, ACT_GELU_TANH = 0, 1, 2
+
+
+def gelu_tanh(x) -> np.ndarray:
+    """GELU in its tanh form, 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), in FP64."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (x + 0.044715 * x * x * x)))
+
+
+def epilogue(acc, alpha=1.0, beta=0.0, c_old=None, bias=None, activation=ACT_NONE) -> np.ndarray:
+    """FP64 value of act(alpha * acc + beta * C_old + bias[col]) before the rounding to BF16.
+
+    acc: FP64 products, M x N. alpha, beta: taken at FP32 precision (the C ABI passes floats).
+    c_old: BF16 bits of the prior C (M x N), read only when beta != 0. bias: BF16 bits, N
+    values (one per column), or None."""
+    alpha = float(np.float32(alpha))
+    beta = float(np.float32(beta))
+    x = alpha * np.asarray(acc, dtype=np.float64)
+    if beta != 0.0:
+        x = x + beta * bf16_bits_to_f64(c_old)
+    if bias is not None:
+        x = x + bf16_bits_to_f64(bias)[None, :]
+    if activation == ACT_RELU:
+        x = np.maximum(x, 0.0)
+    elif activation == ACT_GELU_TANH:
+        x = gelu_tanh(x)
+    elif activation != ACT_NONE:
+        raise ValueError("unknown activation")
+    return x

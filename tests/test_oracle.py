@@ -310,3 +310,79 @@ def test_nvfp4_sampled_and_row_range_agree_with_full():
     rng = np.random.default_rng(2)
     rows, cols = rng.integers(0, 19, 60), rng.integers(0, 23, 60)
     assert np.array_equal(oracle.gemm_nvfp4_at(A, SFA, B, SFB, rows, cols), full[rows, cols])
+
+
+# ---------------------------------------------------------------- fused epilogue
+# Pins for oracle.epilogue: closed forms computed here element by element (BF16 decoded by
+# torch, not by the oracle), the order of the operations, and GELU against an independent
+# formula and against the exact (erf) GELU it approximates.
+
+def _bf16_bits(values):
+    return torch.tensor(values, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bf16_value(bits):
+    t = torch.from_numpy(np.array([bits], dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return float(t.float().item())
+
+
+def test_epilogue_identity():
+    acc = np.random.default_rng(1).standard_normal((4, 6)) * 100
+    assert np.array_equal(oracle.epilogue(acc), acc)
+
+
+def test_epilogue_alpha_beta_bias_closed_form():
+    rng = np.random.default_rng(2)
+    M, N = 3, 5                          # not square: a bias indexed by row would not broadcast
+    acc = rng.standard_normal((M, N)) * 10
+    c_old = _bf16_bits(rng.uniform(-4, 4, (M, N)))
+    bias = _bf16_bits([0.5, -1.0, 2.0, -3.5, 8.0])
+    got = oracle.epilogue(acc, alpha=0.75, beta=-1.5, c_old=c_old, bias=bias)
+    for i in range(M):
+        for j in range(N):
+            want = 0.75 * acc[i, j] + (-1.5) * _bf16_value(c_old[i, j]) + _bf16_value(bias[j])
+            assert got[i, j] == pytest.approx(want, rel=1e-15, abs=1e-15)
+
+
+def test_epilogue_order_of_operations():
+    acc = np.array([[1.0, -1.0]])
+    bias = _bf16_bits([1.0, 2.0])
+    # alpha scales the product only: 2 * 1 + 1 = 3 (not 2 * (1 + 1))
+    assert oracle.epilogue(acc, alpha=2.0, bias=bias)[0, 0] == 3.0
+    # the activation follows the bias: relu(-1 + 2) = 1 (not relu(-1) + 2)
+    assert oracle.epilogue(acc, bias=bias, activation=oracle.ACT_RELU)[0, 1] == 1.0
+
+
+def test_epilogue_beta_zero_does_not_read_c():
+    acc = np.array([[1.0, 2.0]])
+    nan_bits = np.array([[0x7FC0, 0xFFC0]], dtype=np.uint16)
+    assert np.array_equal(oracle.epilogue(acc, alpha=1.0, beta=0.0, c_old=nan_bits), acc)
+
+
+def test_epilogue_relu():
+    acc = np.array([[-3.0, -0.0, 0.0, 2.5]])
+    got = oracle.epilogue(acc, activation=oracle.ACT_RELU)
+    assert list(got[0]) == [0.0, 0.0, 0.0, 2.5]
+
+
+def test_gelu_tanh_against_independent_forms():
+    xs = np.linspace(-8.0, 8.0, 1601)
+    got = oracle.gelu_tanh(xs)
+    # 0.5 (1 + tanh z) = 1 / (1 + exp(-2z)): the same function through a sigmoid
+    import math
+    k = math.sqrt(2.0 / math.pi)
+    for x, g in zip(xs, got):
+        z = k * (x + 0.044715 * x ** 3)
+        assert g == pytest.approx(x / (1.0 + math.exp(-2.0 * z)), rel=1e-12, abs=1e-12)
+        # the exact GELU x Phi(x), which the tanh form approximates to within 1e-3
+        assert abs(g - 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))) < 1e-3
+        # gelu(x) - gelu(-x) = x, since tanh is odd
+    assert np.allclose(oracle.gelu_tanh(xs) - oracle.gelu_tanh(-xs), xs, rtol=0, atol=1e-12)
+    assert oracle.gelu_tanh([0.0])[0] == 0.0
+
+
+def test_epilogue_gelu_dispatch():
+    acc = np.array([[1.0, -2.0]])
+    assert np.array_equal(oracle.epilogue(acc, activation=oracle.ACT_GELU_TANH), oracle.gelu_tanh(acc))
+    with pytest.raises(ValueError):
+        oracle.epilogue(acc, activation=9)

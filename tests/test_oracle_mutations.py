@@ -49,3 +49,39 @@ def test_pins_catch_planted_mistake(name, tmp_path):
                         os.path.join(ROOT, "tests", "test_oracle.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"
+
+
+# The fused epilogue is numpy code in oracle/__init__.py: its mutations edit a copy of the
+# package, which the pin run imports ahead of the real one.
+PY_MUTATIONS = {
+    "bias_indexed_by_row": ("bf16_bits_to_f64(bias)[None, :]", "bf16_bits_to_f64(bias)[:, None]"),
+    "alpha_dropped": ("x = alpha * np.asarray(acc, dtype=np.float64)", "x = np.asarray(acc, dtype=np.float64)"),
+    "beta_sign_flipped": ("x = x + beta * bf16_bits_to_f64(c_old)", "x = x - beta * bf16_bits_to_f64(c_old)"),
+    "relu_ignored": ("x = np.maximum(x, 0.0)", "x = x"),
+    "gelu_cubic_coefficient": ("(x + 0.044715 * x * x * x)", "(x + 0.04715 * x * x * x)"),
+    "gelu_sqrt_two_pi": ("np.sqrt(2.0 / np.pi)", "np.sqrt(2.0 * np.pi)"),
+    "gelu_half_dropped": ("return 0.5 * x * (1.0 + np.tanh(", "return x * (1.0 + np.tanh("),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTATIONS))
+def test_epilogue_pins_catch_planted_mistake(name, tmp_path):
+    import shutil
+    old, new = PY_MUTATIONS[name]
+    pkg = tmp_path / "oracle"
+    shutil.copytree(os.path.join(ROOT, "oracle"), pkg, ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    src = (pkg / "__init__.py").read_text()
+    assert src.count(old) == 1, f"mutation {name} no longer applies to oracle/__init__.py"
+    (pkg / "__init__.py").write_text(src.replace(old, new))
+    sys.path.insert(0, ROOT)
+    import oracle
+    env = dict(os.environ, ORACLE_LIB_OVERRIDE=oracle.build(),
+               PYTHONPATH=os.pathsep.join([str(tmp_path), ROOT, os.environ.get("PYTHONPATH", "")]))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-k", "epilogue or gelu",
+                        os.path.join(ROOT, "tests", "test_oracle.py")],
+                       cwd=str(tmp_path), env=env, capture_output=True, text=True, timeout=600)
+    # the copy must be the one imported (python -m puts the working directory first on sys.path)
+    probe = subprocess.run([sys.executable, "-c", "import oracle; print(oracle.__file__)"], cwd=str(tmp_path), env=env,
+                           capture_output=True, text=True, timeout=120)
+    assert probe.stdout.strip().startswith(str(tmp_path)), probe.stdout + probe.stderr
+    assert r.returncode != 0, f"pins did not catch mutation {name}:\n{r.stdout[-2000:]}"
