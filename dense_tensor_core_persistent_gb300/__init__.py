@@ -41,6 +41,7 @@ EXPORTS = (
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
     "gemm_nvfp4_noalloc", "gemm_measure_mma_rate", "gemm_bf16_fused", "gemm_nvfp4_fused", "gemm_nvfp4_blocked_fused",
+    "gemm_bf16_plan",
 )
 
 # gemm_activation_t
@@ -65,13 +66,15 @@ class gemm_options_t(ctypes.Structure):
         ("debug_flags", ctypes.c_uint32),
         ("no_tail_split", ctypes.c_int),
         ("no_pdl", ctypes.c_int),
-        ("reserved", ctypes.c_int * 2),
+        ("no_swap_ab", ctypes.c_int),
+        ("reserved", ctypes.c_int),
     ]
 
 
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0, no_pdl=0):
-    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl)
+            no_tail_split=0, no_pdl=0, no_swap_ab=0):
+    return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl,
+                          no_swap_ab)
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -138,6 +141,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_nvfp4_fused.restype = I
         l.gemm_nvfp4_blocked_fused.argtypes = [P, P, P, P, P, I, I, I, P, EP, OP]
         l.gemm_nvfp4_blocked_fused.restype = I
+        l.gemm_bf16_plan.argtypes = [I, I, I, OP, EP, ctypes.POINTER(I), ctypes.POINTER(I)]
+        l.gemm_bf16_plan.restype = I
         l.gemm_measure_mma_rate.restype = I
         _lib = l
     return _lib
@@ -244,6 +249,14 @@ def gemm_nvfp4_blocked_fused(A, SFA_blocked, B, SFB_blocked, C, M: int, N: int, 
     _check(lib().gemm_nvfp4_blocked_fused(_ptr(A), _ptr(SFA_blocked), _ptr(B), _ptr(SFB_blocked), _ptr(C), M, N, K,
                                           _stream(stream), _byref_or_null(epi), _byref_or_null(opts)),
            "gemm_nvfp4_blocked_fused")
+
+
+def bf16_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None, epi: gemm_epilogue_t | None = None):
+    """(swap_ab, tile_n) that gemm_bf16 uses for this problem (host only)."""
+    swap, tile_n = ctypes.c_int(), ctypes.c_int()
+    _check(lib().gemm_bf16_plan(M, N, K, _byref_or_null(opts), _byref_or_null(epi), ctypes.byref(swap),
+                                ctypes.byref(tile_n)), "gemm_bf16_plan")
+    return swap.value, tile_n.value
 
 
 def gemm_nvfp4_noalloc(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None) -> None:

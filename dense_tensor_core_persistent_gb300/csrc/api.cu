@@ -170,8 +170,8 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o == nullptr) return GEMM_OK;
-  for (int i = 0; i < 2; ++i)
-    if (o->reserved[i] != 0) return GEMM_ERR_INVALID_ARG;
+  if (o->reserved != 0) return GEMM_ERR_INVALID_ARG;
+  if (o->no_swap_ab != 0 && o->no_swap_ab != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
@@ -184,6 +184,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->max_clusters = o->max_clusters;
   r->tail_split = o->no_tail_split ? 0 : 1;
   r->pdl = o->no_pdl ? 0 : 1;
+  r->swap_ab = o->no_swap_ab ? 0 : 1;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -401,6 +402,18 @@ int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B,
 int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C, int M,
                        int N, int K, void* stream) {
   return gemm_nvfp4_blocked_ex(A, SFA_blocked, B, SFB_blocked, C, M, N, K, stream, nullptr);
+}
+
+int gemm_bf16_plan(int M, int N, int K, const gemm_options_t* options, const gemm_epilogue_t* epilogue, int* swap_ab,
+                   int* tile_n) {
+  if (M < 0 || N < 0 || K < 0 || swap_ab == nullptr || tile_n == nullptr) return GEMM_ERR_INVALID_ARG;
+  RunOptions opt;
+  int st = resolve_options(options, &opt);
+  if (st == GEMM_OK) st = resolve_epilogue(epilogue, &opt.epi);
+  if (st != GEMM_OK) return st;
+  *swap_ab = bf16_swap_ab(M, N, opt) ? 1 : 0;
+  *tile_n = bf16_tile_n(M, N, opt);
+  return GEMM_OK;
 }
 
 const char* gemm_status_string(int status) {

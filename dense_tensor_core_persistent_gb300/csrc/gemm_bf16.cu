@@ -48,10 +48,13 @@ struct Bf16Params {
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
 };
 
-template <int CG, int STAGES, int ATOMS>
+// BN: output columns per tile (the MMA N). SWAP: the kernel computes C^T = B A^T for a
+// GEMM with few rows (its A and B arguments are the caller's B and A) and writes each
+// accumulator chunk transposed into the caller's C.
+template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false>
 struct Bf16Layout {
   static constexpr int BLOCK_M = 128;              // output rows per CTA = TMEM lanes
-  static constexpr int BLOCK_N = 256;              // output columns per tile = MMA N
+  static constexpr int BLOCK_N = BN;               // output columns per tile = MMA N
   static constexpr int ATOM_K = 64;                // BF16 elements of one 128-byte swizzle row
   static constexpr int BLOCK_K = ATOM_K * ATOMS;   // K elements per stage
   static constexpr int UMMA_K = 16;                // K per tcgen05.mma kind::f16
@@ -86,14 +89,15 @@ struct Bf16Layout {
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
   static_assert(TMEM_COLS <= 512, "exceeds the 512 TMEM columns of an SM");
   static_assert(B_ROWS <= 256, "TMA box rows must not exceed 256");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N: 64, 128, 192 or 256 (whole 64-column epilogue chunks)");
 };
 
-template <int CG, int STAGES, int ATOMS>
-__global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
+template <int CG, int STAGES, int ATOMS, int BN, bool SWAP>
+__global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_c,
                      const Bf16Params p) {
-  using L = Bf16Layout<CG, STAGES, ATOMS>;
+  using L = Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // same offset in both CTAs of a pair
@@ -303,7 +307,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
       const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
       const int row0 = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M + static_cast<int>(q) * 32;
       const int col0 = tc.n_blk * L::BLOCK_N + (w.half > 0 ? L::BLOCK_N / 2 : 0);
-      if (p.epi.fused && p.epi.beta != 0.0f && lane == 0 && row0 < p.M) {
+      if (!SWAP && p.epi.fused && p.epi.beta != 0.0f && lane == 0 && row0 < p.M) {
         // the prior C of this warp's part of the tile into L2 while the MMAs still run
         for (int c = 0; c < chunks; ++c)
           if (col0 + c * 64 < p.N) tma_prefetch_l2_2d(&tmap_c, col0 + c * 64, row0);
@@ -327,7 +331,11 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
           // the 128-byte swizzle the C tensor map uses (and bank-conflict free).
           const uint32_t row_addr = buf + lane * 128u;
           uint32_t pk[32];
-          if (!p.epi.fused) {
+          if constexpr (SWAP) {
+            // columns i and 32 + i of this lane's accumulator row, for the transposed tile
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2_rn(lo[i], hi[i]);
+          } else if (!p.epi.fused) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               pk[i] = pack_bf16x2_rn(lo[2 * i], lo[2 * i + 1]);
@@ -369,14 +377,26 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
             // every lane has read its row of the prior C before any lane overwrites it
             __syncwarp();
           }
+          if constexpr (SWAP) {
+            // Transposed staging tile: 64 rows (the chunk's accumulator columns, rows of the
+            // caller's C) x 32 BF16 columns (this warp's accumulator rows). For one row, the
+            // 32 lanes write 64 consecutive bytes: no bank conflicts.
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
-                         pk[4 * j + 2], pk[4 * j + 3]);
+            for (int i = 0; i < 32; ++i) {
+              st_shared_u16(buf + i * 64 + lane * 2, static_cast<uint16_t>(pk[i] & 0xFFFFu));
+              st_shared_u16(buf + (32 + i) * 64 + lane * 2, static_cast<uint16_t>(pk[i] >> 16));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[4 * j], pk[4 * j + 1],
+                           pk[4 * j + 2], pk[4 * j + 3]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmap_c, buf, col, row0);
+            if constexpr (SWAP) tma_store_2d(&tmap_c, buf, row0, col);  // (column, row) of the caller's C
+            else tma_store_2d(&tmap_c, buf, col, row0);
             bulk_commit_group();
           }
           ebuf ^= 1u;
@@ -408,10 +428,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS>::NUM_THREADS, 1)
 
 namespace {
 
-template <int CG, int STAGES, int ATOMS>
+template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false>
 struct Bf16Variant {
-  using L = Bf16Layout<CG, STAGES, ATOMS>;
-  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS>;
+  using L = Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>;
+  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP>;
 
   // Co-resident clusters per device, queried once per device.
   static int max_active_clusters(int device) {
@@ -453,9 +473,14 @@ struct Bf16Variant {
     if (st == GEMM_OK)  // B box of a half-width work item
       st = encode_tmap_2d(&tbh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, K, N, uint64_t(K) * 2, L::ATOM_K,
                           L::B_ROWS / 2, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st == GEMM_OK)
-      st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st == GEMM_OK) {
+      if constexpr (SWAP)  // the caller's C is N x M here: boxes of 64 of its rows x 32 columns
+        st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, M, N, uint64_t(M) * 2, 32, 64,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+      else
+        st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, 64, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (st != GEMM_OK) return st;
 
     Bf16Params p;
@@ -488,7 +513,8 @@ struct Bf16Variant {
       wave = max_clusters;
       if (opt.max_clusters > 0) wave = std::min(wave, opt.max_clusters);
     }
-    p.split_tiles = (opt.persistent && opt.tail_split) ? tail_split_tiles(p.num_tiles, wave) : 0;
+    // (swapped variants keep whole tiles: their tile N is already small)
+    p.split_tiles = (opt.persistent && opt.tail_split && !SWAP) ? tail_split_tiles(p.num_tiles, wave) : 0;
     p.num_items = p.num_tiles + p.split_tiles;
     const int clusters = std::min(p.num_items, wave);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
@@ -521,8 +547,22 @@ struct Bf16Variant {
 using Bf16OneCta = Bf16Variant<1, 4, 1>;
 using Bf16Pair = Bf16Variant<2, 3, 2>;     // 3 stages of 128 K (64 KB per CTA): the default
 using Bf16PairK64 = Bf16Variant<2, 6, 1>;  // 6 stages of 64 K (32 KB per CTA)
+// C^T = B A^T for M <= 64 / M <= 128: tile N 64 / 128, 4 stages of 128 K (40 / 48 KB per CTA)
+using Bf16Swap64 = Bf16Variant<2, 4, 2, 64, true>;
+using Bf16Swap128 = Bf16Variant<2, 4, 2, 128, true>;
 
 }  // namespace
+
+// A GEMM with few rows wastes most of each M = 256 MMA on padding; computed as C^T = B A^T
+// its rows become the MMA's N (64 or 128) and the long N dimension fills the 256 MMA rows.
+bool bf16_swap_ab(int M, int N, const RunOptions& opt) {
+  return opt.swap_ab && opt.kernel == GEMM_KERNEL_DEFAULT && !opt.epi.fused() && M >= 1 && M <= 128 && N >= 256;
+}
+
+int bf16_tile_n(int M, int N, const RunOptions& opt) {
+  if (!bf16_swap_ab(M, N, opt)) return opt.kernel == GEMM_KERNEL_BF16_1CTA ? Bf16OneCta::L::BLOCK_N : Bf16Pair::L::BLOCK_N;
+  return M <= 64 ? Bf16Swap64::L::BLOCK_N : Bf16Swap128::L::BLOCK_N;
+}
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt) {
@@ -533,6 +573,11 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
     case GEMM_KERNEL_BF16_1CTA:
       return Bf16OneCta::run(A, B, C, M, N, K, stream, opt, device, *info);
     case GEMM_KERNEL_DEFAULT:
+      if (bf16_swap_ab(M, N, opt)) {
+        if (M <= 64) return Bf16Swap64::run(B, A, C, N, M, K, stream, opt, device, *info);
+        return Bf16Swap128::run(B, A, C, N, M, K, stream, opt, device, *info);
+      }
+      return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
     case GEMM_KERNEL_BF16_2CTA:
       return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
     case GEMM_KERNEL_BF16_2CTA_K64:

@@ -53,6 +53,7 @@ struct RunOptions {
   int max_clusters = 0;
   int tail_split = 1;
   int pdl = 1;  // programmatic stream serialization on the launch
+  int swap_ab = 1;  // allow C^T = B A^T for BF16 GEMMs with few rows
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
   EpilogueOptions epi;
@@ -60,6 +61,9 @@ struct RunOptions {
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt);
+// Whether run_gemm_bf16 computes C^T = B A^T for this problem, and the tile N it uses.
+bool bf16_swap_ab(int M, int N, const RunOptions& opt);
+int bf16_tile_n(int M, int N, const RunOptions& opt);
 int run_gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                            int M, int N, int K, cudaStream_t stream, const RunOptions& opt);
 int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream, int pdl = 1);

@@ -205,7 +205,11 @@ typedef struct {
     int no_pdl;          /* 0: launch with programmatic stream serialization (the kernel's
                             set-up overlaps the end of the previous kernel on the stream;
                             every global access waits for that kernel); 1: plain launch */
-    int reserved[2];     /* must be zero */
+    int no_swap_ab;      /* BF16, default kernel, no fused epilogue: 0 = a GEMM with M <= 128
+                            and N >= 256 computes C^T = B A^T, so that the few rows of A fill
+                            the MMA's N dimension (64 or 128) instead of padding its 256 rows,
+                            and its epilogue writes C transposed; 1 = never */
+    int reserved;        /* must be zero */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
@@ -287,6 +291,16 @@ int gemm_tile_coord(int M, int N, int tile_m, int tile_n, int group_m, int t, in
  */
 int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_bytes_x2,
                         int concurrent_tiles, long long l2_bytes);
+
+/*
+ * gemm_bf16_plan -- the configuration gemm_bf16_ex / gemm_bf16_fused use for a problem
+ * (host only, no GPU needed): *swap_ab = 1 when the call computes C^T = B A^T (see
+ * gemm_options_t.no_swap_ab), *tile_n = the MMA N of its tiles (256; 64 or 128 when
+ * swapped). options and epilogue may be NULL. Returns GEMM_ERR_INVALID_ARG for negative
+ * sizes, null outputs or invalid options.
+ */
+int gemm_bf16_plan(int M, int N, int K, const gemm_options_t* options, const gemm_epilogue_t* epilogue, int* swap_ab,
+                   int* tile_n);
 
 /* Number of kernel launches this library has issued in this process (all devices). */
 unsigned long long gemm_launch_count(void);

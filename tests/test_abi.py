@@ -50,7 +50,7 @@ def test_argument_errors_are_reported_before_any_device_use():
     assert l.gemm_nvfp4(16, 16, 16, 16, 16, 8, 8, 128, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # K % 256
     assert l.gemm_nvfp4(16, 16, 16, 0, 16, 8, 8, 256, 0) == g.GEMM_ERR_INVALID_ARG
     o = g.options()
-    o.reserved[0] = 1
+    o.reserved = 1
     with pytest.raises(g.GemmError):
         g.gemm_bf16(16, 16, 16, 8, 8, 8, 0, o)
     with pytest.raises(g.GemmError):
@@ -117,3 +117,23 @@ def test_mma_rate_argument_errors():
     out = ctypes.c_double(0.0)
     assert g.lib().gemm_measure_mma_rate(7, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.lib().gemm_measure_mma_rate(g.GEMM_MMA_BF16, None) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_bf16_plan_swaps_few_row_gemms():
+    """C^T = B A^T for M <= 128 and N >= 256 on the default kernel without a fused epilogue."""
+    assert g.bf16_plan(16, 8192, 8192) == (1, 64)
+    assert g.bf16_plan(1, 256, 64) == (1, 64)
+    assert g.bf16_plan(64, 8192, 8192) == (1, 64)
+    assert g.bf16_plan(65, 8192, 8192) == (1, 128)
+    assert g.bf16_plan(128, 8192, 8192) == (1, 128)
+    assert g.bf16_plan(129, 8192, 8192) == (0, 256)
+    assert g.bf16_plan(16, 248, 8192) == (0, 256)          # N too small to fill the MMA rows
+    assert g.bf16_plan(16, 8192, 8192, g.options(no_swap_ab=1)) == (0, 256)
+    assert g.bf16_plan(16, 8192, 8192, g.options(kernel=g.GEMM_KERNEL_BF16_2CTA)) == (0, 256)
+    assert g.bf16_plan(16, 8192, 8192, g.options(kernel=g.GEMM_KERNEL_BF16_1CTA)) == (0, 256)
+    assert g.bf16_plan(16, 8192, 8192, epi=g.epilogue(activation=g.GEMM_ACT_RELU)) == (0, 256)
+    assert g.bf16_plan(16, 8192, 8192, epi=g.epilogue()) == (1, 64)   # the identity epilogue is not fused
+    with pytest.raises(g.GemmError):
+        g.bf16_plan(-1, 8, 8)
+    with pytest.raises(g.GemmError):
+        g.bf16_plan(16, 8192, 8192, g.options(no_swap_ab=2))

@@ -263,3 +263,54 @@ def test_dependent_launches_on_one_stream(no_pdl):
     assert_bf16_close(bits(Y), Y_ref, K, "Y = (A B^T) D^T")
     assert_bf16_close(bits(A2), A2_ref, K, "A2 = D B^T")
     assert_bf16_close(bits(X), X2_ref, K, "X = A2 B^T")
+
+
+# ---------------------------------------------------------------- few-row GEMMs (C^T = B A^T)
+
+SWAP_SHAPES = [
+    (1, 256, 64),        # a matrix-vector product
+    (7, 264, 200),       # ragged N, partial K stage
+    (16, 1024, 320),
+    (64, 520, 1024),     # tile N 64, ragged last 256-row block of the long dimension
+    (65, 776, 136),      # tile N 128
+    (128, 4104, 256),
+]
+
+
+@pytest.mark.parametrize("shape", SWAP_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_swapped_against_oracle(shape):
+    M, N, K = shape
+    swap, tile_n = g.bf16_plan(M, N, K)
+    assert swap == 1 and tile_n == (64 if M <= 64 else 128)
+    A, B = si.bf16_problem(M * 7 + N + K, M, N, K)
+    ref = oracle.gemm_bf16(A, B)
+    assert_bf16_close(run(A, B), ref, K, f"swapped {shape}")
+    assert_bf16_close(run(A, B, no_swap_ab=1), ref, K, f"not swapped {shape}")
+
+
+def test_few_rows_swapped_integer_inputs_bit_exact():
+    M, N, K = 48, 2048, 256
+    A, B = si.bf16_problem(3, M, N, K, kind="int")
+    assert_bf16_exact(run(A, B), oracle.gemm_bf16(A, B), "swapped integer")
+
+
+@pytest.mark.parametrize("max_clusters", [1, 3])
+def test_few_rows_swapped_many_tiles_per_cluster(max_clusters):
+    M, N, K = 32, 8192, 256   # 32 tiles of the long dimension on 1 or 3 clusters
+    A, B = si.bf16_problem(4, M, N, K)
+    assert_bf16_close(run(A, B, max_clusters=max_clusters), oracle.gemm_bf16(A, B), K, f"clusters {max_clusters}")
+
+
+def test_few_rows_swapped_guard_band_untouched():
+    """The transposed stores write nothing outside C."""
+    M, N, K = 40, 520, 128
+    A, B = si.bf16_problem(6, M, N, K)
+    pad = 4096
+    buf = torch.full((M * N + 2 * pad,), 12345.0, dtype=torch.bfloat16, device=DEV)
+    sentinel = bits(buf[:pad]).copy()
+    C = buf[pad:pad + M * N].view(M, N)
+    g.gemm_bf16(A.to(DEV), B.to(DEV), C, M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(buf[:pad]), sentinel)
+    assert np.array_equal(bits(buf[pad + M * N:]), sentinel)
+    assert_bf16_close(bits(C), oracle.gemm_bf16(A, B), K, "guard band")
