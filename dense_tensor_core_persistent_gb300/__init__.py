@@ -67,14 +67,15 @@ class gemm_options_t(ctypes.Structure):
         ("no_tail_split", ctypes.c_int),
         ("no_pdl", ctypes.c_int),
         ("no_swap_ab", ctypes.c_int),
+        ("no_split_k", ctypes.c_int),
         ("reserved", ctypes.c_int),
     ]
 
 
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0, no_pdl=0, no_swap_ab=0):
+            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0):
     return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl,
-                          no_swap_ab)
+                          no_swap_ab, no_split_k)
 
 
 class gemm_epilogue_t(ctypes.Structure):

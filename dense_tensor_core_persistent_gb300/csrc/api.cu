@@ -172,6 +172,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o == nullptr) return GEMM_OK;
   if (o->reserved != 0) return GEMM_ERR_INVALID_ARG;
   if (o->no_swap_ab != 0 && o->no_swap_ab != 1) return GEMM_ERR_INVALID_ARG;
+  if (o->no_split_k != 0 && o->no_split_k != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
@@ -185,6 +186,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->tail_split = o->no_tail_split ? 0 : 1;
   r->pdl = o->no_pdl ? 0 : 1;
   r->swap_ab = o->no_swap_ab ? 0 : 1;
+  r->split_k = o->no_split_k ? 0 : 1;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -196,7 +198,7 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // blocked-scale workspace of gemm_nvfp4. Freed blocks stay in the pool (release threshold
 // at the maximum), so after the first calls the workspace costs no allocation from the
 // driver; blocks freed on one stream are reused by later work on any stream in order.
-static cudaMemPool_t workspace_pool(int device) {
+cudaMemPool_t workspace_pool(int device) {
   static std::mutex mu;
   static cudaMemPool_t pools[64] = {nullptr};
   if (device < 0 || device >= 64) return nullptr;

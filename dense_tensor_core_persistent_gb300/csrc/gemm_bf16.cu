@@ -26,6 +26,7 @@
 // "NVFP4 GEMM on Blackwell" (Kernel 2: leader-owned barriers, cluster-scope waits;
 // Kernel 3: continuous stage/phase counter across tiles and the TMEM-empty handoff).
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -46,7 +47,36 @@ struct Bf16Params {
   unsigned debug_flags;
   int zigzag;  // 1: a cluster's odd-numbered tiles walk K downwards
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
+  // split K (swapped variants): work item i is split i % splits of tile i / splits, over
+  // stages [split * k_per_split, ...); each writes its FP32 partial tile to ws (row r of the
+  // tile at ws + (split * M + r) * ldw); a second kernel sums and rounds them
+  int splits, k_per_split, ldw;
+  float* ws;
 };
+
+struct Bf16Item {
+  int tile, half;  // as WorkItem
+  int split, k0, kn;  // K split, its first stage and its number of stages
+};
+
+__device__ __forceinline__ Bf16Item bf16_item(const Bf16Params& p, int i, bool split_k) {
+  Bf16Item r;
+  if (split_k && p.splits > 1) {
+    r.tile = i / p.splits;
+    r.split = i - r.tile * p.splits;
+    r.half = -1;
+    r.k0 = r.split * p.k_per_split;
+    r.kn = min(p.k_per_split, p.k_iters - r.k0);
+  } else {
+    const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+    r.tile = w.tile;
+    r.half = w.half;
+    r.split = 0;
+    r.k0 = 0;
+    r.kn = p.k_iters;
+  }
+  return r;
+}
 
 // BN: output columns per tile (the MMA N). SWAP: the kernel computes C^T = B A^T for a
 // GEMM with few rows (its A and B arguments are the caller's B and A) and writes each
@@ -160,7 +190,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       bool ok = true;
       int it = 0;
       for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
-        const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+        const Bf16Item w = bf16_item(p, i, SWAP);
         const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
         const bool half = w.half >= 0;
         const bool down = p.zigzag && (it & 1);
@@ -178,10 +208,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         const int row = load_a ? a_row : b_row;
         const bool arm = load_a && (CG == 1 || rank == 0);
 #pragma unroll 2
-        for (int kb = 0; kb < p.k_iters; ++kb) {
+        for (int kb = 0; kb < w.kn; ++kb) {
           // K block of this stage: every other tile of the cluster walks K downwards, so
           // it starts on the K blocks the previous wave of tiles read last (still in L2)
-          const int kblk = down ? p.k_iters - 1 - kb : kb;
+          const int kblk = w.k0 + (down ? w.kn - 1 - kb : kb);
           // swizzle-row columns of this stage that hold any of K (the last block may hold fewer)
           const int atoms = min(ATOMS, (p.K - kblk * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K);
           const uint32_t stage_bytes = atom_bytes * static_cast<uint32_t>(atoms);
@@ -227,7 +257,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       int it = 0;
       const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
       for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
-        const uint32_t idesc = (i >= p.num_tiles - p.split_tiles) ? IDESC_HALF : IDESC_FULL;
+        const Bf16Item w = bf16_item(p, i, SWAP);
+        const uint32_t idesc = w.half >= 0 ? IDESC_HALF : IDESC_FULL;
         const uint32_t slot = static_cast<uint32_t>(it) & 1u;
         const uint32_t acc_phase = (static_cast<uint32_t>(it) >> 1) & 1u;
         if (!wait_phase(bar_tempty + 8 * slot, acc_phase ^ 1u, wctx, status_code(kRoleMma, 0x100 + slot))) {
@@ -241,8 +272,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         // by selects; a full stage issues its MMAs without per-MMA tests (each taken branch
         // costs this thread cycles).
 #pragma unroll 2
-        for (int kb = 0; kb < p.k_iters; ++kb) {
-          const int kblk = down ? p.k_iters - 1 - kb : kb;
+        for (int kb = 0; kb < w.kn; ++kb) {
+          const int kblk = w.k0 + (down ? w.kn - 1 - kb : kb);
           if (!wait_phase(bar_full + 8 * stage, phase, wctx, status_code(kRoleMma, stage))) {
             ok = false;
             break;
@@ -300,7 +331,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     uint32_t ebuf = 0;
     int it = 0;
     for (int i = cluster_idx; i < p.num_items; i += num_clusters, ++it) {
-      const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
+      const Bf16Item w = bf16_item(p, i, SWAP);
       const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
       const int chunks = (w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N) / 64;
       const uint32_t slot = static_cast<uint32_t>(it) & 1u;
@@ -324,6 +355,23 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           tmem_ld_32x32b_x32(taddr + c * 64, lo);
           tmem_ld_32x32b_x32(taddr + c * 64 + 32, hi);
           tmem_ld_wait();
+          if constexpr (SWAP) {
+            if (p.splits > 1) {
+              // a K split: this row's 64 FP32 partial sums of the chunk to the workspace
+              const int row = row0 + static_cast<int>(lane);
+              if (row < p.M) {
+                float4* dst = reinterpret_cast<float4*>(p.ws + (static_cast<size_t>(w.split) * p.M + row) * p.ldw + col);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  dst[j] = make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
+                                       __uint_as_float(lo[4 * j + 2]), __uint_as_float(lo[4 * j + 3]));
+                  dst[8 + j] = make_float4(__uint_as_float(hi[4 * j]), __uint_as_float(hi[4 * j + 1]),
+                                           __uint_as_float(hi[4 * j + 2]), __uint_as_float(hi[4 * j + 3]));
+                }
+              }
+              continue;
+            }
+          }
           const uint32_t buf = stage_base + ebuf * L::EPI_BUF_BYTES;
           if (lane == 0) bulk_wait_group_read<1>();  // the store that last read `buf` is done
           __syncwarp();
@@ -428,6 +476,35 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
 
 namespace {
 
+// Split-K reduction of the swapped GEMM: C[m][n] = bf16_rne(sum over s of ws[s][n][m]), C
+// being the caller's rows x cols BF16 matrix and ws[s] its transpose (cols rows of ldw
+// FP32 values). 32 x 32 tiles through shared memory: reads along m, writes along n.
+__global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __restrict__ ws, uint16_t* __restrict__ C,
+                                                                int rows, int cols, int splits, int ldw) {
+  __shared__ float t[32][33];
+  const int n0 = blockIdx.x * 32, m0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int n = n0 + r, m = m0 + static_cast<int>(threadIdx.x);
+    float acc = 0.0f;
+    if (n < cols && m < rows)
+      for (int s = 0; s < splits; ++s) acc += ws[(static_cast<size_t>(s) * cols + n) * ldw + m];
+    t[r][threadIdx.x] = acc;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += 8) {
+    const int m = m0 + r, n = n0 + static_cast<int>(threadIdx.x);
+    if (m < rows && n < cols) C[static_cast<size_t>(m) * cols + n] = __bfloat16_as_ushort(__float2bfloat16_rn(t[threadIdx.x][r]));
+  }
+}
+
+int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int splits, int ldw, cudaStream_t stream) {
+  const dim3 grid(static_cast<unsigned>(ceil_div(cols, 32)), static_cast<unsigned>(ceil_div(rows, 32)), 1);
+  splitk_reduce_transposed<<<grid, dim3(32, 8, 1), 0, stream>>>(ws, static_cast<uint16_t*>(C), rows, cols, splits, ldw);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+  count_launch();
+  return GEMM_OK;
+}
+
 template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false>
 struct Bf16Variant {
   using L = Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>;
@@ -515,7 +592,19 @@ struct Bf16Variant {
     }
     // (swapped variants keep whole tiles: their tile N is already small)
     p.split_tiles = (opt.persistent && opt.tail_split && !SWAP) ? tail_split_tiles(p.num_tiles, wave) : 0;
-    p.num_items = p.num_tiles + p.split_tiles;
+    // K splits (swapped variants): enough work items to occupy the free clusters. Two
+    // splits did not pay for the reduction pass (at N = K = 8192 the 64 busy SMs already
+    // stream B at the rate the larger grid reaches), so split only 3 ways or more.
+    int splits = 1;
+    if (SWAP && opt.persistent && opt.split_k) {
+      splits = std::min(std::min(wave / std::max(p.num_tiles, 1), 8), p.k_iters / 4);
+      if (splits < 3) splits = 1;
+    }
+    p.k_per_split = ceil_div(p.k_iters, splits);
+    p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split
+    p.ldw = p.num_n_blocks * L::BLOCK_N;
+    p.ws = nullptr;
+    p.num_items = p.splits > 1 ? p.num_tiles * p.splits : p.num_tiles + p.split_tiles;
     const int clusters = std::min(p.num_items, wave);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
@@ -534,13 +623,30 @@ struct Bf16Variant {
     attr[1].val.programmaticStreamSerializationAllowed = opt.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    if (p.splits > 1) {
+      // FP32 partials of every split, from the library's stream-ordered pool
+      cudaMemPool_t pool = workspace_pool(device);
+      void* ws = nullptr;
+      const size_t bytes = static_cast<size_t>(p.splits) * p.M * p.ldw * sizeof(float);
+      if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_OUT_OF_MEMORY;
+      }
+      p.ws = static_cast<float*>(ws);
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tc, p);
+    int st2 = GEMM_OK;
     if (e != cudaSuccess) {
       cudaGetLastError();
-      return GEMM_ERR_LAUNCH;
+      st2 = GEMM_ERR_LAUNCH;
+    } else {
+      count_launch();
     }
-    count_launch();
-    return GEMM_OK;
+    if (p.splits > 1) {
+      if (st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream);
+      if (cudaFreeAsync(p.ws, stream) != cudaSuccess && st2 == GEMM_OK) st2 = GEMM_ERR_LAUNCH;
+    }
+    return st2;
   }
 };
 

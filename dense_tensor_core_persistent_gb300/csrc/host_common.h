@@ -54,10 +54,14 @@ struct RunOptions {
   int tail_split = 1;
   int pdl = 1;  // programmatic stream serialization on the launch
   int swap_ab = 1;  // allow C^T = B A^T for BF16 GEMMs with few rows
+  int split_k = 1;  // allow K splits for the swapped BF16 GEMMs
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
   EpilogueOptions epi;
 };
+
+// The library's stream-ordered memory pool for temporary workspaces (one per device).
+cudaMemPool_t workspace_pool(int device);
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt);

@@ -314,3 +314,36 @@ def test_few_rows_swapped_guard_band_untouched():
     assert np.array_equal(bits(buf[:pad]), sentinel)
     assert np.array_equal(bits(buf[pad + M * N:]), sentinel)
     assert_bf16_close(bits(C), oracle.gemm_bf16(A, B), K, "guard band")
+
+
+# K splits of the swapped GEMM (FP32 partials in a workspace, summed by a second kernel)
+SPLIT_SHAPES = [
+    (16, 1024, 4096),    # 4 tiles, 32 stages: 8 splits
+    (100, 2048, 2048),   # tile N 128, 8 tiles, 16 stages: 4 splits
+    (5, 512, 2056),      # 2 tiles, 17 stages (the last one ragged): 4 splits of 5, 5, 5 and 2
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_split_k_against_oracle(shape):
+    M, N, K = shape
+    A, B = si.bf16_problem(M * 5 + N + K, M, N, K)
+    ref = oracle.gemm_bf16(A, B)
+    before = g.launch_count()
+    got = run(A, B)
+    assert g.launch_count() == before + 2  # the GEMM and the reduction of its K splits
+    assert_bf16_close(got, ref, K, f"split {shape}")
+    assert_bf16_close(run(A, B, no_split_k=1), ref, K, f"swapped, not split {shape}")
+    assert_bf16_close(run(A, B, no_swap_ab=1), ref, K, f"not swapped {shape}")
+
+
+def test_few_rows_split_k_integer_inputs_bit_exact():
+    M, N, K = 32, 1024, 2048   # |partial sums| <= 16 * 2048: exact in FP32, whatever the split
+    A, B = si.bf16_problem(8, M, N, K, kind="int")
+    assert_bf16_exact(run(A, B), oracle.gemm_bf16(A, B), "split integer")
+
+
+def test_few_rows_split_k_with_capped_clusters():
+    M, N, K = 16, 512, 4096    # 2 tiles on 7 clusters: 3 splits of 11, 11 and 10 stages
+    A, B = si.bf16_problem(9, M, N, K)
+    assert_bf16_close(run(A, B, max_clusters=7), oracle.gemm_bf16(A, B), K, "split, 7 clusters")
