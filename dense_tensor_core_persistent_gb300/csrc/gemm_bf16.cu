@@ -17,6 +17,15 @@
 // 230 cycles per stage on the wait, fence and commit besides ~60 per MMA, so with 4 MMAs
 // (512 pipe cycles) per stage it can barely keep the tensor pipe fed.
 //
+// Fused epilogue (gemm_bf16_fused): act(alpha * acc + beta * C + bias) before the rounding;
+// the prior C of a chunk comes by TMA into the staging buffer (epi_pair, common.cuh).
+//
+// Few rows (M <= 128, N >= 256): the host runs the SWAP instantiations on (B, A), so the
+// kernel computes C^T = B A^T with tile N 64 or 128 and its epilogue writes each 64 x 32
+// chunk transposed into C. When such a GEMM has at most a third as many tiles as clusters,
+// its K is split: each split writes FP32 partial sums to a workspace and
+// splitk_reduce_transposed adds them.
+//
 // Design sources: "Achieve cuBLAS Performance on NVIDIA GB300 for HGEMM" (v1 swizzled
 // TMA + descriptor, v3 warp specialisation with full/empty barriers, v4 2-CTA cluster
 // MMA with multicast commit, v5 persistent kernel with a two-slot TMEM pipeline, v6

@@ -23,8 +23,9 @@
  *   - `stream` is a cudaStream_t / CUstream handle (NULL = legacy default
  *     stream). Calls are asynchronous: they enqueue work and return; nothing
  *     is synchronised. Results are visible to later work on `stream`.
- *   - Device memory: gemm_bf16, gemm_nvfp4_blocked and gemm_nvfp4_pack_scales
- *     allocate nothing. gemm_nvfp4 takes a temporary workspace for the
+ *   - Device memory: gemm_nvfp4_blocked and gemm_nvfp4_pack_scales allocate
+ *     nothing; nor does gemm_bf16, except for a few-row GEMM that splits K (see
+ *     gemm_bf16 and gemm_options_t.no_split_k). gemm_nvfp4 takes a temporary workspace for the
  *     rearranged scales from a library-owned, stream-ordered memory pool (see
  *     gemm_nvfp4). The library also holds one process-wide device status word
  *     (a static __device__ variable) that kernels set if a bounded internal
@@ -72,7 +73,10 @@ typedef enum {
  * K == 0: C is set to zero (an empty sum).
  * Kernel: persistent, warp-specialised, 2-CTA (cta_group::2) tcgen05 MMA with
  * a 256 x 256 output tile per CTA pair, double-buffered TMEM accumulator and a
- * TMA-store epilogue; one kernel launch per call.
+ * TMA-store epilogue; one kernel launch per call. With M <= 128 and N >= 256 it
+ * computes C^T = B A^T instead (tile N 64 or 128; see gemm_options_t.no_swap_ab), and
+ * such a GEMM with few tiles splits K: a second launch adds the FP32 partial sums
+ * (workspace from the library's stream-ordered pool, as for gemm_nvfp4; see no_split_k).
  */
 int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* stream);
 
