@@ -347,3 +347,14 @@ def test_few_rows_split_k_with_capped_clusters():
     M, N, K = 16, 512, 4096    # 2 tiles on 7 clusters: 3 splits of 11, 11 and 10 stages
     A, B = si.bf16_problem(9, M, N, K)
     assert_bf16_close(run(A, B, max_clusters=7), oracle.gemm_bf16(A, B), K, "split, 7 clusters")
+
+
+@pytest.mark.parametrize("shape", [(16, 1024, 320), (100, 2056, 4096)], ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_swapped_tile_per_cluster(shape):
+    """persistent = 0: one cluster per tile, no K splits."""
+    M, N, K = shape
+    A, B = si.bf16_problem(M + N, M, N, K)
+    before = g.launch_count()
+    got = run(A, B, persistent=0)
+    assert g.launch_count() == before + 1
+    assert_bf16_close(got, oracle.gemm_bf16(A, B), K, f"tile per cluster {shape}")
