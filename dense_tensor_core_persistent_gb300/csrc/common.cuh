@@ -137,32 +137,71 @@ struct EpiParams {
   int fused;
 };
 
-__device__ __forceinline__ float epi_activation(float x, int act) {
-  if (act == 1) return fmaxf(x, 0.0f);
-  if (act == 2) {
-    // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as
-    // x / (1 + exp(-2u)) (the same function: 0.5 (1 + tanh u) is the logistic function of
-    // 2u), with the exponential intrinsic: a few instructions instead of a tanh expansion.
-    const float u = 0.7978845608028654f * fmaf(0.044715f * x, x * x, x);
-    float r;  // 1 / (1 + exp(-2u)); rcp.approx of +inf (exp overflow) is 0, so x * r = -0
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-2.0f * u)));
-    return x * r;
-  }
-  return x;
+// Two FP32 values in one 64-bit register: the packed forms of mul, fma and add (.f32x2)
+// handle a pair of adjacent columns in one instruction.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;  // rcp.approx of +inf is 0
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 // One pair of adjacent columns: FP32 accumulator bits acc0 / acc1, the prior C and the
-// bias as BF16 pairs (element 0 in the low half).
+// bias as BF16 pairs (element 0 in the low half). x = alpha * acc + beta * C_old + bias,
+// then the activation, then one rounding to BF16.
 __device__ __forceinline__ uint32_t epi_pair(uint32_t acc0, uint32_t acc1, uint32_t old2, uint32_t bias2,
                                              const EpiParams& e) {
-  float x0 = e.alpha * __uint_as_float(acc0), x1 = e.alpha * __uint_as_float(acc1);
-  if (e.beta != 0.0f) {
-    x0 = fmaf(e.beta, __uint_as_float(old2 << 16), x0);
-    x1 = fmaf(e.beta, __uint_as_float(old2 & 0xFFFF0000u), x1);
+  uint64_t x = f2_mul(f2_pack(e.alpha, e.alpha), f2_pack(__uint_as_float(acc0), __uint_as_float(acc1)));
+  if (e.beta != 0.0f)
+    x = f2_fma(f2_pack(e.beta, e.beta), f2_pack(__uint_as_float(old2 << 16), __uint_as_float(old2 & 0xFFFF0000u)), x);
+  x = f2_add(x, f2_pack(__uint_as_float(bias2 << 16), __uint_as_float(bias2 & 0xFFFF0000u)));
+  float y0, y1;
+  if (e.act == 2) {
+    // GELU, tanh form: 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3), evaluated as
+    // x / (1 + exp(-2u)) (the same function: 0.5 (1 + tanh u) is the logistic function of
+    // 2u); exp(-2u) = 2^(t * -2 sqrt(2/pi) / ln 2) with t = x + 0.044715 x^3. If the power
+    // overflows, 1 / inf = 0 and the result is -0.
+    const uint64_t t = f2_fma(f2_mul(x, f2_pack(0.044715f, 0.044715f)), f2_mul(x, x), x);
+    float v0, v1;
+    f2_unpack(f2_mul(t, f2_pack(-2.302208198144325f, -2.302208198144325f)), v0, v1);
+    float d0, d1;
+    f2_unpack(f2_add(f2_pack(ex2_approx(v0), ex2_approx(v1)), f2_pack(1.0f, 1.0f)), d0, d1);
+    f2_unpack(f2_mul(x, f2_pack(rcp_approx(d0), rcp_approx(d1))), y0, y1);
+  } else {
+    f2_unpack(x, y0, y1);
+    if (e.act == 1) {
+      y0 = fmaxf(y0, 0.0f);
+      y1 = fmaxf(y1, 0.0f);
+    }
   }
-  x0 += __uint_as_float(bias2 << 16);
-  x1 += __uint_as_float(bias2 & 0xFFFF0000u);
-  return pack_bf16x2_rn(__float_as_uint(epi_activation(x0, e.act)), __float_as_uint(epi_activation(x1, e.act)));
+  return pack_bf16x2_rn(__float_as_uint(y0), __float_as_uint(y1));
 }
 
 // Bias of 8 consecutive columns starting at `col` (a multiple of 8) as 4 BF16 pairs; zero
