@@ -358,3 +358,17 @@ def test_few_rows_swapped_tile_per_cluster(shape):
     got = run(A, B, persistent=0)
     assert g.launch_count() == before + 1
     assert_bf16_close(got, oracle.gemm_bf16(A, B), K, f"tile per cluster {shape}")
+
+
+@pytest.mark.slow
+def test_c3_8192_cubed_every_element():
+    """The headline configuration in the launch the benchmark times, compared with the
+    oracle on all 67M outputs (the oracle runs in 2048-row blocks, about 25 s of host work)."""
+    M = N = K = 8192
+    A, B = si.bf16_problem(2, M, N, K, device=DEV)
+    C = g.matmul_bf16(A, B)
+    torch.cuda.synchronize()
+    got = bits(C)
+    Ah, Bh = A.cpu(), B.cpu()
+    for r0 in range(0, M, 2048):
+        assert_bf16_close(got[r0:r0 + 2048], oracle.gemm_bf16(Ah, Bh, r0, r0 + 2048), K, f"C3 rows {r0}..")

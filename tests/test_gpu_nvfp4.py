@@ -257,3 +257,17 @@ def test_back_to_back_calls_on_one_stream(no_pdl):
     for (a, sfa, b, sfb), out in zip(probs, outs):
         ref = oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu())
         assert_nvfp4_close(bits(out), ref, "back to back")
+
+
+@pytest.mark.slow
+def test_c5_8192_cubed_every_element():
+    """C5 in the launch the benchmark times (blocked scales), compared with the oracle on all
+    67M outputs, in 2048-row blocks."""
+    M = N = K = 8192
+    a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K, device=DEV)
+    C = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb))
+    torch.cuda.synchronize()
+    got = bits(C)
+    ah, sah, bh, sbh = a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu()
+    for r0 in range(0, M, 2048):
+        assert_nvfp4_close(got[r0:r0 + 2048], oracle.gemm_nvfp4(ah, sah, bh, sbh, r0, r0 + 2048), f"C5 rows {r0}..")
