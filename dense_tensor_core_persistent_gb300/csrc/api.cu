@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -107,35 +108,80 @@ std::atomic<unsigned long long> g_launches{0};
 
 }  // namespace
 
+// Encoded tensor maps of recent calls, per host thread: a map depends only on the
+// parameters in its key (address, type, sizes, strides, box, swizzle), so a repeated call
+// reuses it instead of encoding again (each encode costs the host about half a microsecond,
+// and a call needs up to five).
+namespace {
+struct TmapKey {
+  const void* base;
+  int rank, dtype, swizzle, pad;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3], pad2;
+};
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool valid;
+};
+constexpr int kTmapCacheEntries = 32;
+thread_local TmapEntry t_tmap_cache[kTmapCacheEntries];
+thread_local int t_tmap_next = 0;
+
+int encode_cached(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base, const uint64_t* dims,
+                  const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
+  TmapKey key;
+  std::memset(&key, 0, sizeof(key));  // padding included: keys compare with memcmp
+  key.base = base;
+  key.rank = rank;
+  key.dtype = static_cast<int>(dtype);
+  key.swizzle = static_cast<int>(swizzle);
+  for (int i = 0; i < rank; ++i) key.dims[i] = dims[i];
+  for (int i = 0; i + 1 < rank; ++i) key.strides[i] = strides_bytes[i];
+  for (int i = 0; i < rank; ++i) key.box[i] = box[i];
+  for (TmapEntry& e : t_tmap_cache)
+    if (e.valid && std::memcmp(&e.key, &key, sizeof(key)) == 0) {
+      *map = e.map;
+      return GEMM_OK;
+    }
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return GEMM_ERR_DRIVER;
+  cuuint64_t d[3], st[2];
+  cuuint32_t b[3];
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+  // Out-of-bounds elements of a load are filled with zeros ("NONE" = no NaN request),
+  // which leaves every sum unchanged; out-of-bounds elements of a store are dropped.
+  const CUresult r = fn(map, dtype, rank, const_cast<void*>(base), d, st, b, elem_strides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return GEMM_ERR_DRIVER;
+  TmapEntry& slot = t_tmap_cache[t_tmap_next];
+  t_tmap_next = (t_tmap_next + 1) % kTmapCacheEntries;
+  slot.key = key;
+  slot.map = *map;
+  slot.valid = true;
+  return GEMM_OK;
+}
+}  // namespace
+
 int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner_elems,
                    uint64_t outer_rows, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                    CUtensorMapSwizzle swizzle) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return GEMM_ERR_DRIVER;
-  const cuuint64_t dims[2] = {inner_elems, outer_rows};
-  const cuuint64_t strides[1] = {row_stride_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  // Out-of-bounds elements of a load are filled with zeros ("NONE" = no NaN request),
-  // which leaves every sum unchanged; out-of-bounds elements of a store are dropped.
-  const CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
+  const uint64_t dims[2] = {inner_elems, outer_rows};
+  const uint64_t strides[1] = {row_stride_bytes};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_cached(map, dtype, 2, base, dims, strides, box, swizzle);
 }
 
 int encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t dims[3],
                    const uint64_t strides_bytes[2], const uint32_t box[3], CUtensorMapSwizzle swizzle) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return GEMM_ERR_DRIVER;
-  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-  const cuuint64_t st[2] = {strides_bytes[0], strides_bytes[1]};
-  const cuuint32_t b[3] = {box[0], box[1], box[2]};
-  const cuuint32_t elem_strides[3] = {1, 1, 1};
-  const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, b, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_DRIVER;
+  return encode_cached(map, dtype, 3, base, dims, strides_bytes, box, swizzle);
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
