@@ -372,3 +372,18 @@ def test_c3_8192_cubed_every_element():
     Ah, Bh = A.cpu(), B.cpu()
     for r0 in range(0, M, 2048):
         assert_bf16_close(got[r0:r0 + 2048], oracle.gemm_bf16(Ah, Bh, r0, r0 + 2048), K, f"C3 rows {r0}..")
+
+
+def test_split_k_calls_back_to_back_on_one_stream():
+    """Split-K calls take their workspace from a stream-ordered pool and add it with a second
+    launch: several in a row on one stream, each into its own output."""
+    M, N, K = 16, 1024, 4096
+    probs = [si.bf16_problem(70 + i, M, N, K) for i in range(3)]
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for (A, B), C in zip(probs, outs):
+            g.gemm_bf16(A.to(DEV), B.to(DEV), C, M, N, K, stream=s)
+    s.synchronize()
+    for (A, B), C in zip(probs, outs):
+        assert_bf16_close(bits(C), oracle.gemm_bf16(A, B), K, "back to back")

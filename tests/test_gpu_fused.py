@@ -232,3 +232,42 @@ def test_rejected_epilogues():
         st = l.gemm_nvfp4_blocked_fused(A.data_ptr(), A.data_ptr(), B.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, 256,
                                         None, ctypes.byref(ep), None)
         assert st == want, ("nvfp4", ep.activation, ep.reserved, st)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "nvfp4"])
+@pytest.mark.parametrize("no_pdl", [0, 1])
+def test_beta_reads_the_previous_result_on_one_stream(kind, no_pdl):
+    """Call 1 writes C; call 2 on the same stream reads it as its prior C (beta = 1). With
+    programmatic dependent launch the second kernel starts early, so its prior-C loads must
+    still wait for the first kernel's stores. The expected prior C is call 1's own result
+    (computed once more beforehand: identical launches give identical bits), which may
+    differ from the oracle's rounding by one ulp."""
+    M, N = 512, 1024
+    opts = g.options(no_pdl=no_pdl)
+    s = torch.cuda.Stream()
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    first_c = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    if kind == "bf16":
+        K = 512
+        A1, B1 = (t.to(DEV) for t in si.bf16_problem(61, M, N, K))
+        A2, B2 = si.bf16_problem(62, M, N, K)
+        g.gemm_bf16(A1, B1, first_c, M, N, K, opts=opts)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.gemm_bf16(A1, B1, C, M, N, K, stream=s, opts=opts)
+            g.gemm_bf16_fused(A2.to(DEV), B2.to(DEV), C, M, N, K, g.epilogue(1.0, 1.0), stream=s, opts=opts)
+        s.synchronize()
+        assert_fused_close(bits(C), oracle.gemm_bf16(A2, B2), 1.0, 1.0, bits(first_c), None, g.GEMM_ACT_NONE, K,
+                           "chained")
+    else:
+        K = 1024
+        p1 = [t.to(DEV) for t in si.nvfp4_problem(63, M, N, K)]
+        p2 = [t.to(DEV) for t in si.nvfp4_problem(64, M, N, K)]
+        g.gemm_nvfp4(*p1, first_c, M, N, K, opts=opts)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.gemm_nvfp4(*p1, C, M, N, K, stream=s, opts=opts)
+            g.gemm_nvfp4_fused(*p2, C, M, N, K, g.epilogue(1.0, 1.0), stream=s, opts=opts)
+        s.synchronize()
+        ref = oracle.epilogue(oracle.gemm_nvfp4(*[t.cpu() for t in p2]), 1.0, 1.0, bits(first_c), None)
+        assert_nvfp4_close(bits(C), ref, "chained")
