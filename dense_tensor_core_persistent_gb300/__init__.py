@@ -41,7 +41,7 @@ EXPORTS = (
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
     "gemm_nvfp4_noalloc", "gemm_measure_mma_rate", "gemm_bf16_fused", "gemm_nvfp4_fused", "gemm_nvfp4_blocked_fused",
-    "gemm_bf16_plan",
+    "gemm_bf16_plan", "gemm_clc_rule",
 )
 
 # gemm_activation_t
@@ -68,14 +68,20 @@ class gemm_options_t(ctypes.Structure):
         ("no_pdl", ctypes.c_int),
         ("no_swap_ab", ctypes.c_int),
         ("no_split_k", ctypes.c_int),
-        ("reserved", ctypes.c_int),
+        ("clc", ctypes.c_int),
     ]
 
 
+# gemm_options_t.clc
+GEMM_CLC_AUTO = 0
+GEMM_CLC_ON = 1
+GEMM_CLC_OFF = 2
+
+
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0):
+            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0, clc=GEMM_CLC_AUTO):
     return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl,
-                          no_swap_ab, no_split_k)
+                          no_swap_ab, no_split_k, clc)
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -122,6 +128,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_tile_coord.restype = I
         l.gemm_choose_group_m.argtypes = [I, I, I, I, I, I, I, ctypes.c_longlong]
         l.gemm_choose_group_m.restype = I
+        l.gemm_clc_rule.argtypes = [I, I, I]
+        l.gemm_clc_rule.restype = I
         l.gemm_nvfp4_blocked_scale_bytes.argtypes = [I, I]
         l.gemm_nvfp4_blocked_scale_bytes.restype = ctypes.c_longlong
         l.gemm_nvfp4_pack_scales.argtypes = [P, P, I, I, P]
@@ -287,6 +295,14 @@ def choose_group_m(M, N, K, tile_m, tile_n, elem_bytes_x2, concurrent_tiles, l2_
     if g < 0:
         raise GemmError(-g, "gemm_choose_group_m")
     return g
+
+
+def clc_rule(items: int, wave: int, K: int) -> bool:
+    """Whether a persistent launch with the default options schedules its items with cluster launch control."""
+    r = lib().gemm_clc_rule(items, wave, K)
+    if r < 0:
+        raise GemmError(-r, "gemm_clc_rule")
+    return r == 1
 
 
 def launch_count() -> int:

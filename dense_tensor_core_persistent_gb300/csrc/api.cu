@@ -216,7 +216,7 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o == nullptr) return GEMM_OK;
-  if (o->reserved != 0) return GEMM_ERR_INVALID_ARG;
+  if (o->clc < 0 || o->clc > 2) return GEMM_ERR_INVALID_ARG;
   if (o->no_swap_ab != 0 && o->no_swap_ab != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_split_k != 0 && o->no_split_k != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
@@ -233,6 +233,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->pdl = o->no_pdl ? 0 : 1;
   r->swap_ab = o->no_swap_ab ? 0 : 1;
   r->split_k = o->no_split_k ? 0 : 1;
+  r->clc = o->clc;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -522,6 +523,11 @@ int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_by
   const double per = elem_bytes_x2 * 0.5;
   const double extra = (elem_bytes_x2 == 1) ? 1.0 / 16.0 : 0.0;
   return choose_group_m(M, N, K, tile_m, tile_n, per, extra, concurrent_tiles, l2_bytes);
+}
+
+int gemm_clc_rule(int items, int wave, int K) {
+  if (items < 0 || wave <= 0 || K < 0) return -GEMM_ERR_INVALID_ARG;
+  return clc_rule(items, wave, K) ? 1 : 0;
 }
 
 unsigned long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -126,6 +126,58 @@ __device__ __forceinline__ void settle_after_abort() {
   while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
 }
 
+// ---------------------------------------------------------------- work-item sequence
+
+// A cluster computes a sequence of work items. Static scheduling: its own cluster index,
+// then steps of the number of launched clusters. Cluster launch control (CLC): the grid
+// has one cluster per item; a running cluster starts on its own index and then takes the
+// item of each cluster it cancels before that cluster starts ("NVFP4 GEMM on Blackwell",
+// Kernel 5: the full logical grid is launched and each resident cluster cancels a pending
+// one and takes its tile). Response t of a ring of kClcSlots 16-byte slots names the
+// item after item t of the sequence.
+//
+// One thread of the leader CTA requests response t when it starts item t (once every
+// consumer has released response t - kClcSlots from that slot); the response is written
+// to both CTAs of a pair. Every role that walks the items reads response t when it is
+// done with item t; in each CTA the thread that arms full[s] re-arms it for the next use
+// of the slot, and the others release the slot on the leader's empty[s].
+constexpr int kClcSlots = 4;
+
+struct ClcRing {
+  uint32_t resp;          // this CTA's response slot 0 (slot s at resp + 16 s)
+  uint32_t full;          // this CTA's full[0] (armed with 16 transaction bytes per use)
+  uint32_t empty_leader;  // the leader CTA's empty[0], as a shared::cluster address
+};
+
+// Issuer: request response t (the item after this cluster's item t).
+template <bool MULTICAST>
+__device__ __forceinline__ bool clc_request(const ClcRing& r, uint32_t empty_local, int t, const WaitCtx& w,
+                                            uint32_t code) {
+  const uint32_t s = static_cast<uint32_t>(t) % kClcSlots, ph = (static_cast<uint32_t>(t) / kClcSlots) & 1u;
+  if (!wait_phase(empty_local + 8 * s, ph ^ 1u, w, code)) return false;
+  fence_proxy_async_smem();  // the consumers' reads of the slot before its next asynchronous write
+  clc_try_cancel<MULTICAST>(r.resp + 16 * s, r.full + 8 * s);
+  return true;
+}
+
+// Response t of the slot ring: the next item (the cancelled cluster's first CTA index /
+// cg), or -1 when no cluster was left to cancel or the wait gave up (then ok = false).
+// `arm`: this thread re-arms full[s] for the slot's next use; `release`: it arrives on
+// the leader's empty[s] (every consumer but the issuer).
+__device__ __forceinline__ int clc_next(const ClcRing& r, int t, int cg, bool arm, bool release, const WaitCtx& w,
+                                        uint32_t code, bool& ok) {
+  const uint32_t s = static_cast<uint32_t>(t) % kClcSlots, ph = (static_cast<uint32_t>(t) / kClcSlots) & 1u;
+  if (!wait_phase(r.full + 8 * s, ph, w, code)) {
+    ok = false;
+    return -1;
+  }
+  uint32_t x;
+  const bool got = clc_query(r.resp + 16 * s, x);
+  if (got && arm) mbar_arrive_expect_tx(r.full + 8 * s, 16);
+  if (release) mbar_arrive_cluster_relaxed(r.empty_leader + 8 * s);
+  return got ? static_cast<int>(x) / cg : -1;
+}
+
 // ---------------------------------------------------------------- fused epilogue
 
 // C = act(alpha * acc + beta * C_old + bias[col]), in FP32, rounded once to BF16.

@@ -54,13 +54,15 @@ struct Bf16Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
-  int zigzag;  // 1: a cluster's odd-numbered tiles walk K downwards
+  int zigzag;  // 1: the items of odd-numbered waves (item / wave) walk K downwards
+  int wave;    // co-resident clusters
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
   // split K (swapped variants): work item i is split i % splits of tile i / splits, over
   // stages [split * k_per_split, ...); each writes its FP32 partial tile to ws (row r of the
   // tile at ws + (split * M + r) * ldw); a second kernel sums and rounds them
   int splits, k_per_split, ldw;
   float* ws;
+  int clc;  // 1: one cluster per item is launched; running clusters take the items of clusters they cancel
 };
 
 struct Bf16Item {
@@ -117,9 +119,14 @@ struct Bf16Layout {
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
-  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain, c_loaded[EPI_WARPS]
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 + EPI_WARPS;
-  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain, c_loaded[EPI_WARPS],
+  // clc_full[kClcSlots], clc_empty[kClcSlots]
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 + EPI_WARPS + 2 * kClcSlots;
+  static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // CLC responses, 16 bytes each
+  // releases of a CLC response: producer B of each CTA, the MMA issuer, the epilogue warps
+  // of each CTA, and for a pair producer A of the second CTA (the leader's issues them)
+  static constexpr int CLC_CONSUMERS = CG * (1 + EPI_WARPS) + 1 + (CG - 1);
+  static constexpr int OFF_TMEM_SLOT = OFF_CLC + kClcSlots * 16;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024 bytes
@@ -155,6 +162,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
   const uint32_t bar_never = bar_tempty + 16;        // nobody arrives (timeout-path test)
   const uint32_t bar_drain = bar_never + 8;          // MMA drain after an abort
   const uint32_t bar_cload = bar_drain + 8;          // c_loaded[w]: epilogue warp w's prior-C tile landed
+  const uint32_t bar_clc_full = bar_cload + 8 * L::EPI_WARPS;  // clc_full[s]: CLC response s landed here
+  const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots; // clc_empty[s] (leader): response s released
+  const ClcRing ring{base + L::OFF_CLC, bar_clc_full, CG == 2 ? mapa_shared(bar_clc_empty, 0) : bar_clc_empty};
+  const bool clc = p.clc != 0;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   const WaitCtx wctx{abort_flag, p.status, p.wait_limit_ns};
@@ -171,8 +182,15 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     mbar_init(bar_never, 1);
     mbar_init(bar_drain, 1);
     for (int w = 0; w < L::EPI_WARPS; ++w) mbar_init(bar_cload + 8 * w, 1);
+    for (int t = 0; t < kClcSlots; ++t) {
+      mbar_init(bar_clc_full + 8 * t, 1);
+      mbar_init(bar_clc_empty + 8 * t, L::CLC_CONSUMERS);
+    }
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
+    // every response slot armed for its first use (re-armed by producer A as it reads them)
+    if (clc)
+      for (int t = 0; t < kClcSlots; ++t) mbar_arrive_expect_tx(bar_clc_full + 8 * t, 16);
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
     prefetch_tensormap(&tmap_b_half);
@@ -197,12 +215,20 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool ok = true;
+      const bool issuer = clc && load_a && rank == 0;  // requests the CLC responses
       int it = 0;
-      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
+      for (int i = cluster_idx < p.num_items ? cluster_idx : -1; i >= 0; ++it) {
+        if (issuer && !clc_request<(CG == 2)>(ring, bar_clc_empty, it, wctx, status_code(kRoleProducer, 0x200 + it % kClcSlots))) {
+          ok = false;
+          break;
+        }
         const Bf16Item w = bf16_item(p, i, SWAP);
         const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
         const bool half = w.half >= 0;
-        const bool down = p.zigzag && (it & 1);
+        // K order of the item: every other wave of items walks K downwards, so it starts on
+        // the K blocks the previous wave read last (still in L2). A wave is `wave`
+        // consecutive items: with the static schedule, the items every cluster has at once.
+        const bool down = p.zigzag && ((i / p.wave) & 1);
         const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
         const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
                                                         : static_cast<int>(rank) * L::B_ROWS);
@@ -218,8 +244,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         const bool arm = load_a && (CG == 1 || rank == 0);
 #pragma unroll 2
         for (int kb = 0; kb < w.kn; ++kb) {
-          // K block of this stage: every other tile of the cluster walks K downwards, so
-          // it starts on the K blocks the previous wave of tiles read last (still in L2)
+          // K block of this stage
           const int kblk = w.k0 + (down ? w.kn - 1 - kb : kb);
           // swizzle-row columns of this stage that hold any of K (the last block may hold fewer)
           const int atoms = min(ATOMS, (p.K - kblk * L::BLOCK_K + L::ATOM_K - 1) / L::ATOM_K);
@@ -251,6 +276,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           stage = stage + 1 == STAGES ? 0u : stage + 1;
           phase = stage == 0 ? phase ^ 1u : phase;
         }
+        if (!ok) break;
+        // next item: producer A re-arms this CTA's response slot for its next use
+        i = clc ? clc_next(ring, it, CG, load_a, !issuer, wctx, status_code(kRoleProducer, 0x300 + it % kClcSlots), ok)
+                : (i + num_clusters < p.num_items ? i + num_clusters : -1);
       }
       if (!ok) settle_after_abort();
     }
@@ -265,7 +294,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       if (p.debug_flags & 1u) ok = wait_phase(bar_never, 0, wctx, status_code(kRoleMma, 0xFFFF));
       int it = 0;
       const uint64_t a_desc0 = umma_desc_sw128(base + L::OFF_A), b_desc0 = umma_desc_sw128(base + L::OFF_B);
-      for (int i = cluster_idx; i < p.num_items && ok; i += num_clusters, ++it) {
+      for (int i = cluster_idx < p.num_items ? cluster_idx : -1; i >= 0 && ok; ++it) {
         const Bf16Item w = bf16_item(p, i, SWAP);
         const uint32_t idesc = w.half >= 0 ? IDESC_HALF : IDESC_FULL;
         const uint32_t slot = static_cast<uint32_t>(it) & 1u;
@@ -276,7 +305,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + slot * L::ACC_COLS;
-        const bool down = p.zigzag && (it & 1);  // the producer's K order for this tile
+        const bool down = p.zigzag && ((i / p.wave) & 1);  // the producer's K order for this item
         // Straight-line loop body: descriptors follow from the ring position, which advances
         // by selects; a full stage issues its MMAs without per-MMA tests (each taken branch
         // costs this thread cycles).
@@ -318,6 +347,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         if (!ok) break;
         if constexpr (CG == 1) mma_commit_local(bar_tfull + 8 * slot);
         else mma_commit_pair_multicast(bar_tfull + 8 * slot, 0x3);
+        i = clc ? clc_next(ring, it, CG, false, true, wctx, status_code(kRoleMma, 0x300 + it % kClcSlots), ok)
+                : (i + num_clusters < p.num_items ? i + num_clusters : -1);
       }
       if (!ok) {
         // let issued MMAs finish before TMEM is released
@@ -339,7 +370,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     bool epi_ok = true;
     uint32_t ebuf = 0;
     int it = 0;
-    for (int i = cluster_idx; i < p.num_items; i += num_clusters, ++it) {
+    for (int i = cluster_idx < p.num_items ? cluster_idx : -1; i >= 0; ++it) {
       const Bf16Item w = bf16_item(p, i, SWAP);
       const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
       const int chunks = (w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N) / 64;
@@ -467,6 +498,18 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       if (lane == 0) {
         if constexpr (CG == 2) mbar_arrive_cluster(tempty_target + 8 * slot);
         else mbar_arrive_local(bar_tempty + 8 * slot);
+      }
+      if (clc) {
+        // every lane reads the response; one releases the slot
+        const uint32_t s = static_cast<uint32_t>(it) % kClcSlots, ph = (static_cast<uint32_t>(it) / kClcSlots) & 1u;
+        if (!wait_phase_warp(ring.full + 8 * s, ph, wctx, status_code(kRoleEpilogue, 0x300 + s))) break;
+        uint32_t x;
+        const bool got = clc_query(ring.resp + 16 * s, x);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(ring.empty_leader + 8 * s);
+        i = got ? static_cast<int>(x) / CG : -1;
+      } else {
+        i = i + num_clusters < p.num_items ? i + num_clusters : -1;
       }
     }
     if (lane == 0) bulk_wait_group<0>();
@@ -614,7 +657,10 @@ struct Bf16Variant {
     p.ldw = p.num_n_blocks * L::BLOCK_N;
     p.ws = nullptr;
     p.num_items = p.splits > 1 ? p.num_tiles * p.splits : p.num_tiles + p.split_tiles;
-    const int clusters = std::min(p.num_items, wave);
+    // Cluster launch control: the whole grid of one cluster per item, taken dynamically
+    p.clc = (opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K)) ? 1 : 0;
+    const int clusters = p.clc ? p.num_items : std::min(p.num_items, wave);
+    p.wave = std::max(wave, 1);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
 

@@ -55,6 +55,7 @@ struct RunOptions {
   int pdl = 1;  // programmatic stream serialization on the launch
   int swap_ab = 1;  // allow C^T = B A^T for BF16 GEMMs with few rows
   int split_k = 1;  // allow K splits for the swapped BF16 GEMMs
+  int clc = 0;      // cluster launch control: 0 = by clc_rule, 1 = on, 2 = off
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
   EpilogueOptions epi;

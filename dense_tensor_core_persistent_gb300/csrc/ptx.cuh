@@ -229,6 +229,40 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // are visible; a no-op for a plain launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------- cluster launch control
+
+// Asks the hardware to cancel one cluster of this grid that has not started yet. The
+// 16-byte response lands at `resp` (16-byte aligned) and completes 16 transaction bytes
+// on `bar`; with MULTICAST, at the same offsets in every CTA of the cluster.
+template <bool MULTICAST>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  if constexpr (MULTICAST)
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.multicast::cluster::all.b128 "
+        "[%0], [%1];" ::"r"(resp), "r"(bar) : "memory");
+  else
+    asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                     resp), "r"(bar) : "memory");
+}
+
+// Decodes a response: true if a cluster was cancelled, with the x index of its first CTA.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& first_ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "mov.u32 %1, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t"
+      "}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  first_ctaid_x = x;
+  return ok != 0;
+}
+
 // ---------------------------------------------------------------- register reallocation
 
 // Per-warpgroup register limits: every warp of a warpgroup executes the same call. The

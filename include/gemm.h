@@ -219,7 +219,11 @@ typedef struct {
                             split writes FP32 partial sums to a workspace from the library's
                             stream-ordered pool (as gemm_nvfp4's), and a second kernel adds
                             them and rounds to BF16; 1 = never */
-    int reserved;        /* must be zero */
+    int clc;             /* persistent grids (persistent = 1, max_clusters = 0): 0 = decided by
+                            gemm_clc_rule; 1 = cluster launch control: one cluster per work item
+                            is launched, and each running cluster takes the items of clusters it
+                            cancels before they start (dynamic tile scheduling); 2 = never: the
+                            co-resident clusters walk the items with a fixed stride */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
@@ -277,6 +281,18 @@ int gemm_nvfp4_fused(const void* A, const void* SFA, const void* B, const void* 
 int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                              int M, int N, int K, void* stream, const gemm_epilogue_t* epilogue,
                              const gemm_options_t* options);
+
+/*
+ * gemm_clc_rule -- whether a persistent launch with gemm_options_t.clc = 0 schedules its
+ * work items with cluster launch control (dynamic tile scheduling; "NVFP4 GEMM on
+ * Blackwell", static vs dynamic tile scheduling): items = work items of the launch (tiles,
+ * plus the extra halves of a split tail wave, or tiles x K splits), wave = co-resident
+ * clusters, K = the GEMM's K. Returns 1 when items > wave and K >= 16384, else 0 (a rule
+ * measured on GB300: below that depth the static order, which keeps each SM pair on the
+ * same position of every wave, reads far fewer bytes from DRAM); -GEMM_ERR_INVALID_ARG if
+ * an argument is negative or wave is 0.
+ */
+int gemm_clc_rule(int items, int wave, int K);
 
 /*
  * gemm_tile_coord -- host evaluation of the persistent tile order used by the

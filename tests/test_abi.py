@@ -50,7 +50,7 @@ def test_argument_errors_are_reported_before_any_device_use():
     assert l.gemm_nvfp4(16, 16, 16, 16, 16, 8, 8, 128, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # K % 256
     assert l.gemm_nvfp4(16, 16, 16, 0, 16, 8, 8, 256, 0) == g.GEMM_ERR_INVALID_ARG
     o = g.options()
-    o.reserved = 1
+    o.clc = 3
     with pytest.raises(g.GemmError):
         g.gemm_bf16(16, 16, 16, 8, 8, 8, 0, o)
     with pytest.raises(g.GemmError):
@@ -137,3 +137,22 @@ def test_bf16_plan_swaps_few_row_gemms():
         g.bf16_plan(-1, 8, 8)
     with pytest.raises(g.GemmError):
         g.bf16_plan(16, 8192, 8192, g.options(no_swap_ab=2))
+
+
+def test_clc_rule_bands():
+    """Static / dynamic scheduling: nothing to balance within one wave; beyond it the CLC order
+    only for K >= 16384 (the depth at which it measured faster on GB300, at any wave count)."""
+    W = 76
+    assert not g.clc_rule(1, W, 65536)
+    assert not g.clc_rule(W, W, 65536)            # exactly one wave
+    assert not g.clc_rule(W + 1, W, 16383)
+    assert g.clc_rule(W + 1, W, 16384)
+    assert not g.clc_rule(1024, W, 8192)          # 8192^3 BF16: 1024 tiles of 256 x 256, static
+    assert not g.clc_rule(4096, W, 8192)          # 54 waves, K = 8192: static
+    assert g.clc_rule(1024, W, 16384)
+    assert g.clc_rule(4096, W, 16384)
+    assert not g.clc_rule(256, W, 4096)
+    with pytest.raises(g.GemmError):
+        g.clc_rule(10, 0, 8192)
+    with pytest.raises(g.GemmError):
+        g.clc_rule(-1, W, 8192)

@@ -186,6 +186,16 @@ def test_c4_ragged_4000x14336x4096_sampled():
     _full_size_sampled(3, 4000, 14336, 4096)
 
 
+@pytest.mark.parametrize("shape", [(64, 28672, 8192), (1, 8192, 8192), (128, 8192, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_full_size_sampled(shape):
+    # the swapped path at full depth: a 64-row product over a 28672-wide weight (tile N 64,
+    # 448 tiles), a matrix-vector product (K split over several clusters) and 128 rows
+    M, N, K = shape
+    assert g.bf16_plan(M, N, K)[0] == 1
+    _full_size_sampled(11, M, N, K, n=min(4096, M * N))
+
+
 def test_c3_shape_integer_inputs_sampled_bit_exact():
     # |partial sums| <= 16 * 8192 < 2^24: exact in FP32 at the full size
     _full_size_sampled(2, 8192, 8192, 8192, kind="int", n=8192, exact=True)
