@@ -37,6 +37,7 @@ CONFIGS = {
 # GB300 for HGEMM", Performance table, v7 at M = N = K = 8192 on GB300.
 PAGE_BASELINE = {"c3": 1980.925}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+CLC_MODES = {"auto": 0, "on": 1, "off": 2}   # gemm_options_t.clc
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor rates (6x)
 KERNEL_SOURCES = {
     "bf16": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu"],
@@ -370,7 +371,7 @@ def run_ours(args, cfg, world, rank, local):
     epi = make_epilogue(g, args.epilogue, N, dev)
     opts = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
                      persistent=0 if args.no_persistent else 1, no_tail_split=1 if args.no_tail_split else 0,
-                     no_pdl=1 if args.no_pdl else 0)
+                     no_pdl=1 if args.no_pdl else 0, clc=CLC_MODES[args.clc])
     flops = 2.0 * M * N * K
     torch.cuda.synchronize()
 
@@ -525,6 +526,9 @@ def run_ours(args, cfg, world, rank, local):
                        "blocked tensor-core layout (packed once at input setup)" if args.scales == "blocked"
                        else "row-major [rows][K/16], packed to the tensor-core layout inside each call"),
             "group_m": args.group_m or "auto",
+            "scheduler": {"auto": "default (gemm_clc_rule: cluster launch control only for BF16 beyond one wave "
+                                  "with K >= 16384)", "on": "cluster launch control",
+                          "off": "static grid stride"}[args.clc],
             "epilogue": ("plain BF16 rounding" if args.epilogue == "none" else
                          f"fused {args.epilogue}: alpha, beta, bias, activation = {EPILOGUES[args.epilogue]}"
                          + (" (e2e: the prior C is the device buffer's previous contents)"
@@ -566,6 +570,8 @@ def main():
     ap.add_argument("--max-clusters", type=int, default=0)
     ap.add_argument("--no-persistent", action="store_true")
     ap.add_argument("--no-tail-split", action="store_true")
+    ap.add_argument("--clc", default="auto", choices=sorted(CLC_MODES),
+                    help="tile scheduler: the default rule, cluster launch control, or the static grid stride")
     ap.add_argument("--scales", default="blocked", choices=["blocked", "rowmajor"])
     ap.add_argument("--epilogue", default="none", choices=sorted(EPILOGUES),
                     help="fused epilogue of the *_fused calls (default: the plain GEMM)")

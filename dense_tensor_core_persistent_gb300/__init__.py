@@ -128,7 +128,7 @@ def lib() -> ctypes.CDLL:
         l.gemm_tile_coord.restype = I
         l.gemm_choose_group_m.argtypes = [I, I, I, I, I, I, I, ctypes.c_longlong]
         l.gemm_choose_group_m.restype = I
-        l.gemm_clc_rule.argtypes = [I, I, I]
+        l.gemm_clc_rule.argtypes = [I, I, I, I]
         l.gemm_clc_rule.restype = I
         l.gemm_nvfp4_blocked_scale_bytes.argtypes = [I, I]
         l.gemm_nvfp4_blocked_scale_bytes.restype = ctypes.c_longlong
@@ -297,9 +297,9 @@ def choose_group_m(M, N, K, tile_m, tile_n, elem_bytes_x2, concurrent_tiles, l2_
     return g
 
 
-def clc_rule(items: int, wave: int, K: int) -> bool:
+def clc_rule(items: int, wave: int, K: int, nvfp4: bool = False) -> bool:
     """Whether a persistent launch with the default options schedules its items with cluster launch control."""
-    r = lib().gemm_clc_rule(items, wave, K)
+    r = lib().gemm_clc_rule(items, wave, K, int(nvfp4))
     if r < 0:
         raise GemmError(-r, "gemm_clc_rule")
     return r == 1

@@ -525,9 +525,9 @@ int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_by
   return choose_group_m(M, N, K, tile_m, tile_n, per, extra, concurrent_tiles, l2_bytes);
 }
 
-int gemm_clc_rule(int items, int wave, int K) {
-  if (items < 0 || wave <= 0 || K < 0) return -GEMM_ERR_INVALID_ARG;
-  return clc_rule(items, wave, K) ? 1 : 0;
+int gemm_clc_rule(int items, int wave, int K, int nvfp4) {
+  if (items < 0 || wave <= 0 || K < 0 || (nvfp4 != 0 && nvfp4 != 1)) return -GEMM_ERR_INVALID_ARG;
+  return clc_rule(items, wave, K, nvfp4 != 0) ? 1 : 0;
 }
 
 unsigned long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

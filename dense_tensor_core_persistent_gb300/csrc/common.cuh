@@ -149,12 +149,19 @@ struct ClcRing {
   uint32_t empty_leader;  // the leader CTA's empty[0], as a shared::cluster address
 };
 
+// INLINE: the waits are inlined (for roles running under a changed register limit).
+template <bool INLINE>
+__device__ __forceinline__ bool clc_wait(uint32_t bar, uint32_t parity, const WaitCtx& w, uint32_t code) {
+  if constexpr (INLINE) return wait_phase_inline(bar, parity, w, code);
+  else return wait_phase(bar, parity, w, code);
+}
+
 // Issuer: request response t (the item after this cluster's item t).
-template <bool MULTICAST>
+template <bool MULTICAST, bool INLINE = false>
 __device__ __forceinline__ bool clc_request(const ClcRing& r, uint32_t empty_local, int t, const WaitCtx& w,
                                             uint32_t code) {
   const uint32_t s = static_cast<uint32_t>(t) % kClcSlots, ph = (static_cast<uint32_t>(t) / kClcSlots) & 1u;
-  if (!wait_phase(empty_local + 8 * s, ph ^ 1u, w, code)) return false;
+  if (!clc_wait<INLINE>(empty_local + 8 * s, ph ^ 1u, w, code)) return false;
   fence_proxy_async_smem();  // the consumers' reads of the slot before its next asynchronous write
   clc_try_cancel<MULTICAST>(r.resp + 16 * s, r.full + 8 * s);
   return true;
@@ -164,10 +171,11 @@ __device__ __forceinline__ bool clc_request(const ClcRing& r, uint32_t empty_loc
 // cg), or -1 when no cluster was left to cancel or the wait gave up (then ok = false).
 // `arm`: this thread re-arms full[s] for the slot's next use; `release`: it arrives on
 // the leader's empty[s] (every consumer but the issuer).
+template <bool INLINE = false>
 __device__ __forceinline__ int clc_next(const ClcRing& r, int t, int cg, bool arm, bool release, const WaitCtx& w,
                                         uint32_t code, bool& ok) {
   const uint32_t s = static_cast<uint32_t>(t) % kClcSlots, ph = (static_cast<uint32_t>(t) / kClcSlots) & 1u;
-  if (!wait_phase(r.full + 8 * s, ph, w, code)) {
+  if (!clc_wait<INLINE>(r.full + 8 * s, ph, w, code)) {
     ok = false;
     return -1;
   }

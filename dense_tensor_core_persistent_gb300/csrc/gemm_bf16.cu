@@ -658,7 +658,7 @@ struct Bf16Variant {
     p.ws = nullptr;
     p.num_items = p.splits > 1 ? p.num_tiles * p.splits : p.num_tiles + p.split_tiles;
     // Cluster launch control: the whole grid of one cluster per item, taken dynamically
-    p.clc = (opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K)) ? 1 : 0;
+    p.clc = (opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K, false)) ? 1 : 0;
     const int clusters = p.clc ? p.num_items : std::min(p.num_items, wave);
     p.wave = std::max(wave, 1);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)

@@ -61,7 +61,9 @@ struct Nvfp4Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
-  int zigzag;     // 1: a cluster's odd-numbered tiles walk K downwards
+  int zigzag;     // 1: the items of odd-numbered waves (item / wave) walk K downwards
+  int wave;       // co-resident clusters
+  int clc;        // 1: one cluster per item is launched; running clusters take the items of clusters they cancel
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
 };
 
@@ -108,11 +110,15 @@ struct Nvfp4Layout {
   static constexpr int EPI_COLS = 16;
   static constexpr int EPI_BUF_BYTES = 32 * EPI_COLS * 2;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUF_BYTES;
-  // full[S], empty[S], sf_ready[S], tmem_full, tmem_empty, never, drain
   // full[S], empty[S], sf_ready[S], sf_free[SF_SMEM_STAGES], tmem_full, tmem_empty, never, drain,
-  // c_loaded[EPI_WARPS]
-  static constexpr int NUM_BARS = 3 * STAGES + SF_SMEM_STAGES + 4 + EPI_WARPS;
-  static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
+  // c_loaded[EPI_WARPS], clc_full[kClcSlots], clc_empty[kClcSlots]
+  static constexpr int NUM_BARS = 3 * STAGES + SF_SMEM_STAGES + 4 + EPI_WARPS + 2 * kClcSlots;
+  static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // CLC responses, 16 bytes each
+  // releases of a CLC response: producers B and SF and the epilogue warps of both CTAs, the
+  // MMA issuer and the copiers (leader), and producer A of the second CTA (the leader's
+  // issues the requests)
+  static constexpr int CLC_CONSUMERS = CG * (2 + EPI_WARPS) + 1 + COPY_WARPS + 1;
+  static constexpr int OFF_TMEM_SLOT = OFF_CLC + kClcSlots * 16;
   static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
   static constexpr int SMEM_USED = OFF_ABORT + 4;
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
@@ -131,11 +137,26 @@ struct Nvfp4Layout {
 struct Nvfp4Ctx {
   uint32_t base;       // 1024-aligned shared-memory base (same offset in both CTAs)
   uint32_t warp, lane, rank;
-  int cluster_idx, num_clusters, my_items;
+  int cluster_idx, num_clusters;
   uint32_t tmem_base;
   uint32_t bar_full, bar_empty, bar_sfready, bar_sffree, bar_tfull, bar_tempty, bar_never, bar_drain, bar_cload;
+  uint32_t bar_clc_empty;  // this CTA's clc_empty[0] (the leader's are the ones used)
+  ClcRing ring;
+  bool clc;
   WaitCtx wctx;
 };
+
+// First item of this cluster and the item after item `it` (static stride or CLC response
+// `it`). `arm` / `release` as for clc_next; the roles here run under changed register
+// limits, so the waits are inlined.
+__device__ __forceinline__ int nvfp4_first_item(const Nvfp4Params& p, const Nvfp4Ctx& x) {
+  return x.cluster_idx < p.num_items ? x.cluster_idx : -1;
+}
+__device__ __forceinline__ int nvfp4_next_item(const Nvfp4Params& p, const Nvfp4Ctx& x, int i, int it, bool arm,
+                                               bool release, uint32_t code, bool& ok) {
+  if (x.clc) return clc_next<true>(x.ring, it, 2, arm, release, x.wctx, code, ok);
+  return i + x.num_clusters < p.num_items ? i + x.num_clusters : -1;
+}
 
 // ---------------------------------------------------------------- TMA producers (both CTAs)
 // warp 0: A (and the leader arms the full barrier with the bytes of both CTAs); warp 1: B;
@@ -151,14 +172,20 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
   uint32_t stage = 0, phase = 0;
   uint32_t sf_stage = 0, sf_phase = 0;  // the scale producer's slot in the scale ring
   bool ok = true;
+  const bool is_a = x.warp == L::WARP_PROD_A;
+  const bool issuer = x.clc && is_a && x.rank == 0;  // requests the CLC responses
   int it = 0;
-  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
+  for (int i = nvfp4_first_item(p, x); i >= 0; ++it) {
+    if (issuer && !clc_request<true, true>(x.ring, x.bar_clc_empty, it, x.wctx, status_code(kRoleProducer, 0x500 + it % kClcSlots))) {
+      ok = false;
+      break;
+    }
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
     const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
     const bool half = w.half >= 0;
-    // every other tile of the cluster walks K downwards, so it starts on the K blocks the
-    // previous wave of tiles read last (still in L2)
-    const bool down = p.zigzag && (it & 1);
+    // every other wave of items walks K downwards, so it starts on the K blocks the
+    // previous wave read last (still in L2)
+    const bool down = p.zigzag && ((i / p.wave) & 1);
     const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(x.rank) * L::BLOCK_M;
     const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(x.rank) * (L::B_ROWS / 2)
                                                     : static_cast<int>(x.rank) * L::B_ROWS);
@@ -170,7 +197,6 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
     // selects): A and B issue one 2-D copy per stage, the scale producer a 2-D and a 3-D one.
     if (x.warp != L::WARP_PROD_SF) {
       static_assert(L::A_BYTES == L::B_BYTES, "A and B stages share one stride");
-      const bool is_a = x.warp == L::WARP_PROD_A;
       const bool arm = is_a && x.rank == 0;  // one arrival with the bytes of both CTAs
       const uint32_t dst0 = x.base + (is_a ? L::OFF_A : L::OFF_B);
       const CUtensorMap* map = is_a ? tmap_a : map_b;
@@ -210,6 +236,9 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
         sf_phase = sf_stage == 0 ? sf_phase ^ 1u : sf_phase;
       }
     }
+    if (!ok) break;
+    // producer A re-arms this CTA's response slot for its next use
+    i = nvfp4_next_item(p, x, i, it, is_a, !issuer, status_code(kRoleProducer, 0x600 + it % kClcSlots), ok);
   }
   if (!ok) settle_after_abort();
 }
@@ -225,7 +254,6 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
   using L = Nvfp4Layout<STAGES>;
   if (x.rank != 0 || x.lane != 0) return;
   const uint32_t c = x.warp - L::COPY_WARP0;
-  const long long total = static_cast<long long>(x.my_items > 0 ? x.my_items : 0) * p.k_iters;
   const uint64_t sfa0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFA, 128), c * L::SF_BLOCK);
   const uint64_t sfb0 = umma_desc_advance(umma_desc_plain(x.base + L::OFF_SFB, 128), c * L::SF_BLOCK);
   const uint32_t col0 = x.tmem_base + L::SF_TMEM_COL0;
@@ -233,22 +261,15 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
   uint32_t sf_smem = 0;               // scale ring in shared memory
   uint32_t sf_stage = 0;              // scale ring in TMEM
   uint32_t e_stage = 0, e_phase = 0;  // A/B ring position of stage g - SF_STAGES
-  bool ok = true;
-  // straight-line loop body: the ring positions advance by selects
-#pragma unroll 2
-  for (long long g = 0; g < total; ++g) {
-    if (!wait_phase_inline(x.bar_full + 8 * stage, phase, x.wctx, status_code(kRoleScales, 0x300 + stage))) {
-      ok = false;
-      break;
-    }
+  // Stage g (counted over all of this cluster's items): false if a wait gave up.
+  auto copy_stage = [&](long long g) -> bool {
+    if (!wait_phase_inline(x.bar_full + 8 * stage, phase, x.wctx, status_code(kRoleScales, 0x300 + stage))) return false;
     if constexpr (L::SF_STAGES < STAGES) {
       // The TMEM slot's previous stage (g - SF_STAGES) must have completed its MMAs, which
       // read the scales there. (With equal rings the producers' wait implies it.)
       if (g >= L::SF_STAGES) {
-        if (!wait_phase_inline(x.bar_empty + 8 * e_stage, e_phase, x.wctx, status_code(kRoleScales, 0x400 + e_stage))) {
-          ok = false;
-          break;
-        }
+        if (!wait_phase_inline(x.bar_empty + 8 * e_stage, e_phase, x.wctx, status_code(kRoleScales, 0x400 + e_stage)))
+          return false;
         e_stage = e_stage + 1 == STAGES ? 0u : e_stage + 1;
         e_phase = e_stage == 0 ? e_phase ^ 1u : e_phase;
       }
@@ -272,6 +293,35 @@ __device__ __forceinline__ void copier_role(const Nvfp4Params& p, const Nvfp4Ctx
     phase = stage == 0 ? phase ^ 1u : phase;
     sf_smem = sf_smem + 1 == L::SF_SMEM_STAGES ? 0u : sf_smem + 1;
     sf_stage = sf_stage + 1 == L::SF_STAGES ? 0u : sf_stage + 1;
+    return true;
+  };
+  bool ok = true;
+  if (!x.clc) {
+    // static schedule: this cluster's stage count is known, one straight-line loop over all
+    // of them (a per-item loop around it measured 2.7% slower)
+    const int items = x.cluster_idx < p.num_items ? (p.num_items - x.cluster_idx + x.num_clusters - 1) / x.num_clusters : 0;
+    const long long total = static_cast<long long>(items) * p.k_iters;
+#pragma unroll 2
+    for (long long g = 0; g < total; ++g) {
+      if (!copy_stage(g)) {
+        ok = false;
+        break;
+      }
+    }
+  } else {
+    long long g = 0;
+    int it = 0;
+    for (int i = nvfp4_first_item(p, x); i >= 0; ++it) {
+#pragma unroll 2
+      for (int kb = 0; kb < p.k_iters; ++kb, ++g) {
+        if (!copy_stage(g)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+      i = nvfp4_next_item(p, x, i, it, false, true, status_code(kRoleScales, 0x600 + it % kClcSlots), ok);
+    }
   }
   if (!ok) settle_after_abort();
 }
@@ -315,7 +365,7 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
   const uint64_t a_desc0 = umma_desc_sw128(x.base + L::OFF_A), b_desc0 = umma_desc_sw128(x.base + L::OFF_B);
   const uint32_t sf_col0 = x.tmem_base + L::SF_TMEM_COL0;
   int it = 0;
-  for (int i = x.cluster_idx; i < p.num_items && ok; i += x.num_clusters, ++it) {
+  for (int i = nvfp4_first_item(p, x); i >= 0 && ok; ++it) {
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
     const uint32_t idesc = w.half >= 0 ? IDESC_HALF : IDESC_FULL;
     const uint32_t sfb_half_col = w.half > 0 ? 4u : 0u;  // scale columns of the item's N-half
@@ -355,6 +405,7 @@ __device__ __forceinline__ void mma_role(const Nvfp4Params& p, const Nvfp4Ctx& x
     }
     if (!ok) break;
     mma_commit_pair_multicast(x.bar_tfull, 0x3);
+    i = nvfp4_next_item(p, x, i, it, false, true, status_code(kRoleMma, 0x600 + it % kClcSlots), ok);
   }
   if (!ok) {
     mma_commit_pair_multicast(x.bar_drain, 0x1);
@@ -381,7 +432,7 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
   uint32_t cload_phase = 0;
   bool epi_ok = true;
   int it = 0;
-  for (int i = x.cluster_idx; i < p.num_items && epi_ok; i += x.num_clusters, ++it) {
+  for (int i = nvfp4_first_item(p, x); i >= 0; ++it) {
     const WorkItem w = work_item(i, p.num_tiles, p.split_tiles);
     const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
     const int width = w.half >= 0 ? L::BLOCK_N / 2 : L::BLOCK_N;  // accumulator columns of the item
@@ -464,6 +515,20 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
         }
       }
     }
+    if (!epi_ok) break;
+    if (x.clc) {
+      // every lane reads the response; one releases the slot
+      const uint32_t s = static_cast<uint32_t>(it) % kClcSlots, ph = (static_cast<uint32_t>(it) / kClcSlots) & 1u;
+      if (__all_sync(0xffffffffu, wait_phase_inline(x.ring.full + 8 * s, ph, x.wctx, status_code(kRoleEpilogue, 0x600 + s))) == 0)
+        break;
+      uint32_t cx;
+      const bool got = clc_query(x.ring.resp + 16 * s, cx);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(x.ring.empty_leader + 8 * s);
+      i = got ? static_cast<int>(cx) / L::CG : -1;
+    } else {
+      i = i + x.num_clusters < p.num_items ? i + x.num_clusters : -1;
+    }
   }
   if (lane == 0) bulk_wait_group<0>();
   __syncwarp();
@@ -480,7 +545,9 @@ __device__ __forceinline__ void teardown(const Nvfp4Ctx& x) {
   }
 }
 
-template <int STAGES, bool FUSED>
+// CLC: the instantiation with cluster launch control (p.clc == 1); the static one holds none
+// of its code (the roles' tests of x.clc fold away).
+template <int STAGES, bool FUSED, bool CLC>
 __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_sfa,
@@ -497,7 +564,6 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   x.rank = cluster_ctarank();
   x.cluster_idx = static_cast<int>(blockIdx.x) / L::CG;
   x.num_clusters = static_cast<int>(gridDim.x) / L::CG;
-  x.my_items = (p.num_items - x.cluster_idx + x.num_clusters - 1) / x.num_clusters;
   x.bar_full = x.base + L::OFF_BAR;             // stage landed (leader's, bytes of both CTAs)
   x.bar_empty = x.bar_full + 8 * STAGES;        // stage consumed by the MMAs (both CTAs)
   x.bar_sfready = x.bar_empty + 8 * STAGES;     // stage's scales copied to TMEM (leader's)
@@ -507,6 +573,10 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   x.bar_never = x.bar_tempty + 8;               // nobody arrives (timeout-path test)
   x.bar_drain = x.bar_never + 8;                // MMA drain after an abort
   x.bar_cload = x.bar_drain + 8;                // c_loaded[w]: epilogue warp w's prior-C tile landed
+  const uint32_t bar_clc_full = x.bar_cload + 8 * L::EPI_WARPS;  // CLC response s landed here
+  x.bar_clc_empty = bar_clc_full + 8 * kClcSlots;                // CLC response s released (leader's)
+  x.ring = ClcRing{x.base + L::OFF_CLC, bar_clc_full, mapa_shared(x.bar_clc_empty, 0)};
+  x.clc = CLC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   x.wctx = WaitCtx{abort_flag, p.status, p.wait_limit_ns};
@@ -523,8 +593,15 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     mbar_init(x.bar_never, 1);
     mbar_init(x.bar_drain, 1);
     for (int w = 0; w < L::EPI_WARPS; ++w) mbar_init(x.bar_cload + 8 * w, 1);
+    for (int t = 0; t < kClcSlots; ++t) {
+      mbar_init(bar_clc_full + 8 * t, 1);
+      mbar_init(x.bar_clc_empty + 8 * t, L::CLC_CONSUMERS);
+    }
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
+    // every response slot armed for its first use (re-armed by producer A as it reads them)
+    if (x.clc)
+      for (int t = 0; t < kClcSlots; ++t) mbar_arrive_expect_tx(bar_clc_full + 8 * t, 16);
     prefetch_tensormap(&tmap_a);
     prefetch_tensormap(&tmap_b);
     prefetch_tensormap(&tmap_b_half);
@@ -572,8 +649,10 @@ namespace {
 
 constexpr int kStages = 6;
 using NL = Nvfp4Layout<kStages>;
-constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kStages, false>;
-constexpr auto kNvfp4KernelFused = nvfp4_gemm_kernel<kStages, true>;
+constexpr auto kNvfp4Kernel = nvfp4_gemm_kernel<kStages, false, false>;
+constexpr auto kNvfp4KernelFused = nvfp4_gemm_kernel<kStages, true, false>;
+constexpr auto kNvfp4KernelClc = nvfp4_gemm_kernel<kStages, false, true>;
+constexpr auto kNvfp4KernelFusedClc = nvfp4_gemm_kernel<kStages, true, true>;
 
 int max_active_clusters(int device) {
   static std::mutex mu;
@@ -581,10 +660,8 @@ int max_active_clusters(int device) {
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= 64) return 0;
   if (cache[device] > 0) return cache[device];
-  if (cudaFuncSetAttribute(kNvfp4Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) != cudaSuccess ||
-      cudaFuncSetAttribute(kNvfp4KernelFused, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) !=
-          cudaSuccess)
-    return 0;
+  for (auto k : {kNvfp4Kernel, kNvfp4KernelFused, kNvfp4KernelClc, kNvfp4KernelFusedClc})
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, NL::SMEM_BYTES) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(2 * 16, 1, 1);
@@ -675,7 +752,10 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   }
   p.split_tiles = (opt.persistent && opt.tail_split) ? tail_split_tiles(p.num_tiles, wave) : 0;
   p.num_items = p.num_tiles + p.split_tiles;
-  const int clusters = std::min(p.num_items, wave);
+  // Cluster launch control: the whole grid of one cluster per item, taken dynamically
+  p.clc = (opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K, true)) ? 1 : 0;
+  const int clusters = p.clc ? p.num_items : std::min(p.num_items, wave);
+  p.wave = std::max(wave, 1);
   // bytes per row element: half a byte of code; plus one scale byte per 16 elements
   p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                               : choose_group_m(M, N, K, NL::TILE_M, NL::BLOCK_N, 0.5, 1.0 / 16.0, clusters,
@@ -695,7 +775,8 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   attr[1].val.programmaticStreamSerializationAllowed = opt.pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const auto kernel = p.epi.fused ? kNvfp4KernelFused : kNvfp4Kernel;
+  const auto kernel = p.clc ? (p.epi.fused ? kNvfp4KernelFusedClc : kNvfp4KernelClc)
+                            : (p.epi.fused ? kNvfp4KernelFused : kNvfp4Kernel);
   cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tsa, tsb, tc, p);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -72,17 +72,19 @@ DTCP_HD int tail_split_tiles(int num_tiles, int clusters) {
 // Whether a persistent launch of `items` work items, with `wave` co-resident clusters and
 // depth K, schedules them dynamically with cluster launch control (CLC) rather than by a
 // fixed grid stride. Within one wave there is nothing to balance. Beyond it, measured on
-// GB300 (BF16, 2304 to 16384 on a side): with K = 16384 or more the dynamic order gains
-// 0.6-2%; with K up to 12288 it loses 3-14%, also at 4 to 54 waves. Both orders run the same
-// items at the same time, but the dynamic one changes which SM pair computes which tile of
-// a wave, and the launch then reads up to 2.8x as many bytes from DRAM. ("NVFP4 GEMM on
-// Blackwell", static vs dynamic tile scheduling, settled on CLC from four waves on and, for
-// one to four waves, only for K >= 16384; the K condition is the one that holds here.)
-DTCP_HD bool clc_rule(int items, int wave, int K) { return items > wave && K >= 16384; }
+// GB300 (2304 to 16384 on a side): both orders run the same items at the same time, but
+// the dynamic one changes which SM pair computes which tile of a wave, and the launch then
+// reads up to 2.8x as many bytes from DRAM. For BF16 that costs 3-14% with K up to 12288
+// (also at 4 to 54 waves), while with K = 16384 or more the dynamic order gains 0.6-2%.
+// For NVFP4 it gained nowhere beyond noise (K = 32768 at 4096^2: 0.5%) and lost up to 13%
+// (16384^3), so NVFP4 keeps the static order. ("NVFP4 GEMM on Blackwell", static vs dynamic
+// tile scheduling, settled on CLC from four waves on and, for one to four waves, only for
+// K >= 16384, for another kernel on another GPU.)
+DTCP_HD bool clc_rule(int items, int wave, int K, bool nvfp4) { return !nvfp4 && items > wave && K >= 16384; }
 
 // mode: 0 = clc_rule, 1 = always, 2 = never.
-DTCP_HD bool use_clc(int mode, int items, int wave, int K) {
-  return mode == 1 ? true : (mode == 2 ? false : clc_rule(items, wave, K));
+DTCP_HD bool use_clc(int mode, int items, int wave, int K, bool nvfp4) {
+  return mode == 1 ? true : (mode == 2 ? false : clc_rule(items, wave, K, nvfp4));
 }
 
 }  // namespace dtcp

@@ -287,12 +287,13 @@ int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void*
  * work items with cluster launch control (dynamic tile scheduling; "NVFP4 GEMM on
  * Blackwell", static vs dynamic tile scheduling): items = work items of the launch (tiles,
  * plus the extra halves of a split tail wave, or tiles x K splits), wave = co-resident
- * clusters, K = the GEMM's K. Returns 1 when items > wave and K >= 16384, else 0 (a rule
- * measured on GB300: below that depth the static order, which keeps each SM pair on the
- * same position of every wave, reads far fewer bytes from DRAM); -GEMM_ERR_INVALID_ARG if
- * an argument is negative or wave is 0.
+ * clusters, K = the GEMM's K, nvfp4 = 1 for the NVFP4 kernel, 0 for BF16. Returns 1 for a
+ * BF16 launch with items > wave and K >= 16384, else 0 (a rule measured on GB300: below
+ * that depth, and for NVFP4 at the depths measured, the static order, which keeps each SM
+ * pair on the same position of every wave, reads far fewer bytes from DRAM);
+ * -GEMM_ERR_INVALID_ARG if an argument is negative, wave is 0 or nvfp4 is not 0 or 1.
  */
-int gemm_clc_rule(int items, int wave, int K);
+int gemm_clc_rule(int items, int wave, int K, int nvfp4);
 
 /*
  * gemm_tile_coord -- host evaluation of the persistent tile order used by the

@@ -141,7 +141,7 @@ def test_bf16_plan_swaps_few_row_gemms():
 
 def test_clc_rule_bands():
     """Static / dynamic scheduling: nothing to balance within one wave; beyond it the CLC order
-    only for K >= 16384 (the depth at which it measured faster on GB300, at any wave count)."""
+    only for BF16 with K >= 16384 (where it measured faster on GB300, at any wave count)."""
     W = 76
     assert not g.clc_rule(1, W, 65536)
     assert not g.clc_rule(W, W, 65536)            # exactly one wave
@@ -152,6 +152,9 @@ def test_clc_rule_bands():
     assert g.clc_rule(1024, W, 16384)
     assert g.clc_rule(4096, W, 16384)
     assert not g.clc_rule(256, W, 4096)
+    # NVFP4 keeps the static order at every depth
+    assert not g.clc_rule(1024, W, 16384, nvfp4=True)
+    assert not g.clc_rule(4096, W, 65536, nvfp4=True)
     with pytest.raises(g.GemmError):
         g.clc_rule(10, 0, 8192)
     with pytest.raises(g.GemmError):

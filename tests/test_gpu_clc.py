@@ -117,6 +117,59 @@ def test_clc_nvfp4_against_oracle():
     assert_nvfp4_close(bits(C), oracle.gemm_nvfp4(a, sfa, b, sfb), "clc nvfp4")
 
 
+def test_clc_nvfp4_fused_and_static_agree():
+    from test_gpu_fused import bias_bits, prior_c, to_dev_bf16
+    M, N, K = 2304, 3072, 512
+    a, sfa, b, sfb = (t.to(DEV) for t in si.nvfp4_problem(13, M, N, K))
+    bias = to_dev_bf16(bias_bits(N, 14))
+    c_old = to_dev_bf16(prior_c(M, N, 15))
+    outs = []
+    for mode in (CLC, g.GEMM_CLC_OFF):
+        C = c_old.clone()
+        g.gemm_nvfp4_fused(a, sfa, b, sfb, C, M, N, K, g.epilogue(0.75, 0.5, bias, g.GEMM_ACT_GELU_TANH),
+                           opts=g.options(clc=mode))
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_clc_nvfp4_deep_k_sampled():
+    # K = 16384 (64 stages per item) with more tiles than co-resident pairs
+    M, N, K = 2304, 3072, 16384
+    a, sfa, b, sfb = si.nvfp4_problem(16, M, N, K)
+    C = g.matmul_nvfp4(a.to(DEV), sfa.to(DEV), b.to(DEV), sfb.to(DEV), opts=g.options(clc=CLC))
+    torch.cuda.synchronize()
+    rows, cols = sample_coords(M, N, 2048, 16)
+    assert_nvfp4_close(bits(C)[rows, cols], oracle.gemm_nvfp4_at(a, sfa, b, sfb, rows, cols), "nvfp4 deep K")
+
+
+def test_clc_bf16_deep_k_default_schedule():
+    # the default options take the CLC order here (BF16, 108 tiles, K = 16384)
+    M, N, K = 2304, 3072, 16384
+    assert g.clc_rule(108, 76, K)
+    A, B = si.bf16_problem(18, M, N, K, device=DEV)
+    C = g.matmul_bf16(A, B)
+    C_static = g.matmul_bf16(A, B, opts=g.options(clc=g.GEMM_CLC_OFF))
+    torch.cuda.synchronize()
+    assert torch.equal(C, C_static)
+    rows, cols = sample_coords(M, N, 2048, 18)
+    assert_bf16_close(bits(C)[rows, cols], oracle.gemm_bf16_at(A.cpu(), B.cpu(), rows, cols), K, "bf16 deep K")
+
+
+def test_clc_nvfp4_bounded_wait_reports_timeout():
+    g.get_device_status()
+    M, N, K = 2304, 3072, 512
+    a, sfa, b, sfb = (t.to(DEV) for t in si.nvfp4_problem(17, M, N, K))
+    g.matmul_nvfp4(a, sfa, b, sfb, opts=g.options(clc=CLC, wait_limit_us=100_000, debug_flags=1))
+    st, _ = g.get_device_status()
+    assert st == g.GEMM_ERR_TIMEOUT
+    C = g.matmul_nvfp4(a, sfa, b, sfb, opts=g.options(clc=CLC))
+    C_static = g.matmul_nvfp4(a, sfa, b, sfb, opts=g.options(clc=g.GEMM_CLC_OFF))
+    torch.cuda.synchronize()
+    assert torch.equal(C, C_static)
+    assert g.get_device_status()[0] == g.GEMM_OK
+
+
 def test_clc_back_to_back_on_one_stream():
     M, N, K = 2304, 3072, 192
     A, B = si.bf16_problem(12, M, N, K, device=DEV)
