@@ -530,10 +530,14 @@ namespace {
 
 // Split-K reduction of the swapped GEMM: C[m][n] = bf16_rne(sum over s of ws[s][n][m]), C
 // being the caller's rows x cols BF16 matrix and ws[s] its transpose (cols rows of ldw
-// FP32 values). 32 x 32 tiles through shared memory: reads along m, writes along n.
+// FP32 values). 32 x 32 tiles through shared memory: reads along m, writes along n. Launched
+// with programmatic stream serialization: its blocks start while the GEMM drains and wait
+// for it (griddepcontrol.wait) before the first read.
 __global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __restrict__ ws, uint16_t* __restrict__ C,
                                                                 int rows, int cols, int splits, int ldw) {
   __shared__ float t[32][33];
+  pdl_launch_dependents();
+  pdl_wait();
   const int n0 = blockIdx.x * 32, m0 = blockIdx.y * 32;
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int n = n0 + r, m = m0 + static_cast<int>(threadIdx.x);
@@ -549,10 +553,22 @@ __global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __r
   }
 }
 
-int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int splits, int ldw, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>(ceil_div(cols, 32)), static_cast<unsigned>(ceil_div(rows, 32)), 1);
-  splitk_reduce_transposed<<<grid, dim3(32, 8, 1), 0, stream>>>(ws, static_cast<uint16_t*>(C), rows, cols, splits, ldw);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int splits, int ldw, cudaStream_t stream,
+                         int pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(cols, 32)), static_cast<unsigned>(ceil_div(rows, 32)), 1);
+  cfg.blockDim = dim3(32, 8, 1);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, splitk_reduce_transposed, ws, static_cast<uint16_t*>(C), rows, cols, splits, ldw) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
   count_launch();
   return GEMM_OK;
 }
@@ -698,7 +714,7 @@ struct Bf16Variant {
       count_launch();
     }
     if (p.splits > 1) {
-      if (st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream);
+      if (st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream, opt.pdl);
       if (cudaFreeAsync(p.ws, stream) != cudaSuccess && st2 == GEMM_OK) st2 = GEMM_ERR_LAUNCH;
     }
     return st2;
