@@ -54,7 +54,7 @@ struct Bf16Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
-  int zigzag;  // 1: the items of odd-numbered waves (item / wave) walk K downwards
+  int zigzag;  // 1: the items of odd-numbered waves walk K downwards
   int wave;    // co-resident clusters
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
   // split K (swapped variants): work item i is split i % splits of tile i / splits, over
@@ -138,7 +138,9 @@ struct Bf16Layout {
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "tile N: 64, 128, 192 or 256 (whole 64-column epilogue chunks)");
 };
 
-template <int CG, int STAGES, int ATOMS, int BN, bool SWAP>
+// CLC: the instantiation with cluster launch control (p.clc == 1); the static one holds none
+// of its code.
+template <int CG, int STAGES, int ATOMS, int BN, bool SWAP, bool CLC>
 __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_c,
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
   const uint32_t bar_clc_full = bar_cload + 8 * L::EPI_WARPS;  // clc_full[s]: CLC response s landed here
   const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots; // clc_empty[s] (leader): response s released
   const ClcRing ring{base + L::OFF_CLC, bar_clc_full, CG == 2 ? mapa_shared(bar_clc_empty, 0) : bar_clc_empty};
-  const bool clc = p.clc != 0;
+  constexpr bool clc = CLC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
   const WaitCtx wctx{abort_flag, p.status, p.wait_limit_ns};
@@ -226,9 +228,9 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         const TileCoord tc = tile_coord(w.tile, p.num_m_blocks, p.num_n_blocks, p.group_m);
         const bool half = w.half >= 0;
         // K order of the item: every other wave of items walks K downwards, so it starts on
-        // the K blocks the previous wave read last (still in L2). A wave is `wave`
-        // consecutive items: with the static schedule, the items every cluster has at once.
-        const bool down = p.zigzag && ((i / p.wave) & 1);
+        // the K blocks the previous wave read last (still in L2). Static schedule: a cluster's
+        // item count is the wave number. CLC: the wave is item / co-resident clusters.
+        const bool down = p.zigzag && (((clc ? i / p.wave : it) & 1) != 0);
         const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(rank) * L::BLOCK_M;
         const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(rank) * (L::B_ROWS / 2)
                                                         : static_cast<int>(rank) * L::B_ROWS);
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + slot * L::ACC_COLS;
-        const bool down = p.zigzag && ((i / p.wave) & 1);  // the producer's K order for this item
+        const bool down = p.zigzag && (((clc ? i / p.wave : it) & 1) != 0);  // the producer's K order for this item
         // Straight-line loop body: descriptors follow from the ring position, which advances
         // by selects; a full stage issues its MMAs without per-MMA tests (each taken branch
         // costs this thread cycles).
@@ -576,7 +578,8 @@ int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int split
 template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false>
 struct Bf16Variant {
   using L = Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>;
-  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP>;
+  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, false>;
+  static constexpr auto kernel_clc = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, true>;
 
   // Co-resident clusters per device, queried once per device.
   static int max_active_clusters(int device) {
@@ -585,7 +588,8 @@ struct Bf16Variant {
     std::lock_guard<std::mutex> lock(mu);
     if (device < 0 || device >= 64) return 0;
     if (cache[device] > 0) return cache[device];
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(kernel_clc, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM_BYTES) != cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -705,7 +709,7 @@ struct Bf16Variant {
       }
       p.ws = static_cast<float*>(ws);
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tbh, tc, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, p.clc ? kernel_clc : kernel, ta, tb, tbh, tc, p);
     int st2 = GEMM_OK;
     if (e != cudaSuccess) {
       cudaGetLastError();

@@ -61,7 +61,7 @@ struct Nvfp4Params {
   unsigned* status;
   unsigned long long wait_limit_ns;
   unsigned debug_flags;
-  int zigzag;     // 1: the items of odd-numbered waves (item / wave) walk K downwards
+  int zigzag;     // 1: the items of odd-numbered waves walk K downwards
   int wave;       // co-resident clusters
   int clc;        // 1: one cluster per item is launched; running clusters take the items of clusters they cancel
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
@@ -185,7 +185,7 @@ __device__ __forceinline__ void producer_role(const Nvfp4Params& p, const CUtens
     const bool half = w.half >= 0;
     // every other wave of items walks K downwards, so it starts on the K blocks the
     // previous wave read last (still in L2)
-    const bool down = p.zigzag && ((i / p.wave) & 1);
+    const bool down = p.zigzag && (((x.clc ? i / p.wave : it) & 1) != 0);
     const int a_row = tc.m_blk * L::TILE_M + static_cast<int>(x.rank) * L::BLOCK_M;
     const int b_row = tc.n_blk * L::BLOCK_N + (half ? w.half * (L::BLOCK_N / 2) + static_cast<int>(x.rank) * (L::B_ROWS / 2)
                                                     : static_cast<int>(x.rank) * L::B_ROWS);
