@@ -392,6 +392,21 @@ def run_ours(args, cfg, world, rank, local):
     if clocks:
         clocks.wait_first_sample()
 
+    graph, graph_launches = None, 0
+    if args.graph:
+        # the K timed steps captured once into a CUDA graph (the library's launches become
+        # kernel nodes, with programmatic dependencies where the launches ask for them), then
+        # replayed once untimed before the timed replay
+        launches_c0 = g.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for i in range(args.steps):
+                launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
+        graph_launches = g.launch_count() - launches_c0
+        with torch.cuda.stream(stream):
+            graph.replay()
+        stream.synchronize()
+
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -400,15 +415,19 @@ def run_ours(args, cfg, world, rank, local):
     if clocks:
         clocks.mark_start()
     ev0.record(stream)
-    for i in range(args.steps):
-        launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            graph.replay()
+    else:
+        for i in range(args.steps):
+            launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
     ev1.record(stream)
     stream.synchronize()
     if clocks:
         clocks.mark_end()
     torch.cuda.synchronize()
     barrier(world)
-    launches = g.launch_count() - launches0
+    launches = graph_launches if graph is not None else g.launch_count() - launches0
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
     st, detail = g.get_device_status(stream)
@@ -526,6 +545,7 @@ def run_ours(args, cfg, world, rank, local):
                        "blocked tensor-core layout (packed once at input setup)" if args.scales == "blocked"
                        else "row-major [rows][K/16], packed to the tensor-core layout inside each call"),
             "group_m": args.group_m or "auto",
+            "launch": "one CUDA graph replay of the timed steps" if args.graph else "one library call per step from the host",
             "scheduler": {"auto": "default (gemm_clc_rule: cluster launch control only for BF16 beyond one wave "
                                   "with K >= 16384)", "on": "cluster launch control",
                           "off": "static grid stride"}[args.clc],
@@ -570,6 +590,8 @@ def main():
     ap.add_argument("--max-clusters", type=int, default=0)
     ap.add_argument("--no-persistent", action="store_true")
     ap.add_argument("--no-tail-split", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time one replay of a CUDA graph holding the K steps instead of K launches from the host")
     ap.add_argument("--clc", default="auto", choices=sorted(CLC_MODES),
                     help="tile scheduler: the default rule, cluster launch control, or the static grid stride")
     ap.add_argument("--scales", default="blocked", choices=["blocked", "rowmajor"])
