@@ -245,6 +245,24 @@ def launch(g, cfg, ins, C, stream, opts, scales="blocked", epi=None):
         g.gemm_nvfp4(ins[0], ins[1], ins[2], ins[3], C, M, N, K, stream, opts)
 
 
+def cpu_model() -> str:
+    """The host CPU's model, from /proc/cpuinfo (x86: "model name"; Arm: implementer and part codes)."""
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        arm_parts = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd0c": "Neoverse N1", "0xd49": "Neoverse N2"}
+        part = fields.get("CPU part", "?")
+        return f"Arm implementer {fields.get('CPU implementer', '?')} part {part} ({arm_parts.get(part, 'unknown part')})"
+    except OSError:
+        return "unknown"
+
+
 def oracle_rows(cfg, ins_cpu, rows):
     import oracle
     if cfg["kind"] == "bf16":
@@ -270,7 +288,8 @@ def cpu_baseline(cfg, target_s=10.0):
     oracle_rows(cfg, ins_cpu, rows)
     dt = time.perf_counter() - t
     flops = 2.0 * rows * N * K
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "cpu": cpu_model(),
+            "kind": "oracle",
             "sample": f"first {rows} of {M} rows of C (all {N} columns, K={K}), FP64, {dt:.1f} s",
             "seconds": dt, "rows": rows}
 
@@ -337,8 +356,8 @@ def run_reference(args, cfg, world, rank):
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": cfg["workload"], "M": M, "N": N, "K": K, "sample_per_step": sample},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "cpu": cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

@@ -192,3 +192,22 @@ def test_clc_bounded_wait_reports_timeout_and_context_survives():
     A2, B2 = si.bf16_problem(1, 2304, 3072, 192)
     assert_bf16_close(run(A2, B2, clc=CLC), oracle.gemm_bf16(A2, B2), 192, "after timeout")
     assert g.get_device_status()[0] == g.GEMM_OK
+
+
+def test_clc_option_defers_to_capped_and_one_tile_per_cluster_grids():
+    # CLC applies to uncapped persistent grids; with a cluster cap or one cluster per tile
+    # the request is ignored and the static walk runs
+    M, N, K = 2304, 3072, 192
+    A, B = si.bf16_problem(19, M, N, K)
+    ref = oracle.gemm_bf16(A, B)
+    assert_bf16_close(run(A, B, clc=CLC, max_clusters=5), ref, K, "clc with a cluster cap")
+    assert_bf16_close(run(A, B, clc=CLC, persistent=0), ref, K, "clc with one cluster per tile")
+
+
+def test_clc_call_is_one_launch():
+    A, B = si.bf16_problem(20, 2304, 3072, 192, device=DEV)
+    torch.cuda.synchronize()
+    before = g.launch_count()
+    g.matmul_bf16(A, B, opts=g.options(clc=CLC))
+    torch.cuda.synchronize()
+    assert g.launch_count() == before + 1
