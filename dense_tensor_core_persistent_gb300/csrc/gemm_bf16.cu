@@ -532,26 +532,40 @@ namespace {
 
 // Split-K reduction of the swapped GEMM: C[m][n] = bf16_rne(sum over s of ws[s][n][m]), C
 // being the caller's rows x cols BF16 matrix and ws[s] its transpose (cols rows of ldw
-// FP32 values). 32 x 32 tiles through shared memory: reads along m, writes along n. Launched
-// with programmatic stream serialization: its blocks start while the GEMM drains and wait
-// for it (griddepcontrol.wait) before the first read.
+// FP32 values). 32 x 32 tiles through shared memory: reads along m, writes along n. Every
+// thread issues all of its loads (4 rows x up to kMaxSplits splits) before the first add,
+// so they overlap instead of each waiting for the previous one. Launched with
+// programmatic stream serialization: its blocks start while the GEMM drains and wait for
+// it (griddepcontrol.wait) before the first read.
+constexpr int kMaxSplits = 8;
+
 __global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __restrict__ ws, uint16_t* __restrict__ C,
                                                                 int rows, int cols, int splits, int ldw) {
   __shared__ float t[32][33];
   pdl_launch_dependents();
   pdl_wait();
   const int n0 = blockIdx.x * 32, m0 = blockIdx.y * 32;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int n = n0 + r, m = m0 + static_cast<int>(threadIdx.x);
+  const int m = m0 + static_cast<int>(threadIdx.x);
+  float v[4][kMaxSplits];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + static_cast<int>(threadIdx.y) + 8 * i;
+    const bool in = n < cols && m < rows;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      v[i][s] = (in && s < splits) ? __ldg(ws + (static_cast<size_t>(s) * cols + n) * ldw + m) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
     float acc = 0.0f;
-    if (n < cols && m < rows)
-      for (int s = 0; s < splits; ++s) acc += ws[(static_cast<size_t>(s) * cols + n) * ldw + m];
-    t[r][threadIdx.x] = acc;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) acc += v[i][s];  // in split order, as before
+    t[threadIdx.y + 8 * i][threadIdx.x] = acc;
   }
   __syncthreads();
   for (int r = threadIdx.y; r < 32; r += 8) {
-    const int m = m0 + r, n = n0 + static_cast<int>(threadIdx.x);
-    if (m < rows && n < cols) C[static_cast<size_t>(m) * cols + n] = __bfloat16_as_ushort(__float2bfloat16_rn(t[threadIdx.x][r]));
+    const int mm = m0 + r, n = n0 + static_cast<int>(threadIdx.x);
+    if (mm < rows && n < cols) C[static_cast<size_t>(mm) * cols + n] = __bfloat16_as_ushort(__float2bfloat16_rn(t[threadIdx.x][r]));
   }
 }
 
@@ -664,13 +678,15 @@ struct Bf16Variant {
     }
     // (swapped variants keep whole tiles: their tile N is already small)
     p.split_tiles = (opt.persistent && opt.tail_split && !SWAP) ? tail_split_tiles(p.num_tiles, wave) : 0;
-    // K splits (swapped variants): enough work items to occupy the free clusters. Two
-    // splits did not pay for the reduction pass (at N = K = 8192 the 64 busy SMs already
-    // stream B at the rate the larger grid reaches), so split only 3 ways or more.
+    // K splits (swapped variants): enough work items to occupy the free clusters. A split
+    // costs about 4 us (FP32 partials out and back, the reduction kernel), so two splits pay
+    // only where halving the per-pair stream saves more: tile N 64 and at least 48 stages
+    // (measured at N = K = 8192: 34.1 -> 31.2 us for M = 64; tile N 128 and K = 2048 lost).
     int splits = 1;
     if (SWAP && opt.persistent && opt.split_k) {
-      splits = std::min(std::min(wave / std::max(p.num_tiles, 1), 8), p.k_iters / 4);
-      if (splits < 3) splits = 1;
+      splits = std::min(std::min(wave / std::max(p.num_tiles, 1), kMaxSplits), p.k_iters / 4);
+      const bool two_pay = BN == 64 && p.k_iters >= 48;
+      if (splits < 2 || (splits == 2 && !two_pay)) splits = 1;
     }
     p.k_per_split = ceil_div(p.k_iters, splits);
     p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split

@@ -213,12 +213,12 @@ typedef struct {
                             and N >= 256 computes C^T = B A^T, so that the few rows of A fill
                             the MMA's N dimension (64 or 128) instead of padding its 256 rows,
                             and its epilogue writes C transposed; 1 = never */
-    int no_split_k;      /* swapped BF16 GEMMs with at most a third as many tiles as clusters:
-                            0 = split K over 3 to 8 clusters per tile (at least 4 stages of
-                            128 K each); each
-                            split writes FP32 partial sums to a workspace from the library's
-                            stream-ordered pool (as gemm_nvfp4's), and a second kernel adds
-                            them and rounds to BF16; 1 = never */
+    int no_split_k;      /* swapped BF16 GEMMs with at most half as many tiles as clusters:
+                            0 = split K over 2 to 8 clusters per tile (at least 4 stages of
+                            128 K each; two splits only for tile N 64 with at least 48 stages);
+                            each split writes FP32 partial sums to a workspace from the
+                            library's stream-ordered pool (as gemm_nvfp4's), and a second
+                            kernel adds them and rounds to BF16; 1 = never */
     int clc;             /* persistent grids (persistent = 1, max_clusters = 0): 0 = decided by
                             gemm_clc_rule; 1 = cluster launch control: one cluster per work item
                             is launched, and each running cluster takes the items of clusters it

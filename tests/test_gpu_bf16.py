@@ -331,6 +331,7 @@ SPLIT_SHAPES = [
     (16, 1024, 4096),    # 4 tiles, 32 stages: 8 splits
     (100, 2048, 2048),   # tile N 128, 8 tiles, 16 stages: 4 splits
     (5, 512, 2056),      # 2 tiles, 17 stages (the last one ragged): 4 splits of 5, 5, 5 and 2
+    (4, 8192, 6144),     # tile N 64, 32 tiles, 48 stages: 2 splits
 ]
 
 
@@ -345,6 +346,17 @@ def test_few_rows_split_k_against_oracle(shape):
     assert_bf16_close(got, ref, K, f"split {shape}")
     assert_bf16_close(run(A, B, no_split_k=1), ref, K, f"swapped, not split {shape}")
     assert_bf16_close(run(A, B, no_swap_ab=1), ref, K, f"not swapped {shape}")
+
+
+def test_few_rows_two_splits_only_where_they_pay():
+    # 32 tiles of 256 rows: two splits for tile N 64 with 48 stages or more, none otherwise
+    for (M, N, K, launches) in [(4, 8192, 6144, 2), (4, 8192, 5632, 1), (100, 8192, 8192, 1)]:
+        A, B = si.bf16_problem(M + K, M, N, K, device=DEV)
+        torch.cuda.synchronize()
+        before = g.launch_count()
+        g.matmul_bf16(A, B)
+        torch.cuda.synchronize()
+        assert g.launch_count() == before + launches, (M, N, K)
 
 
 def test_few_rows_split_k_integer_inputs_bit_exact():
