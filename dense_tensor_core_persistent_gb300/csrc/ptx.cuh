@@ -14,12 +14,6 @@ namespace dtcp {
 
 // ---------------------------------------------------------------- special registers
 
-__device__ __forceinline__ uint32_t lane_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%laneid;" : "=r"(r));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -368,24 +362,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(uint32_t lo_bits, uint32_t hi
   return d;
 }
 
-// Same conversion, kept in program order with the other volatile asm (TMEM loads): lets
-// a caller bound how many loaded-but-unconverted registers are live at once.
-__device__ __forceinline__ uint32_t pack_bf16x2_rn_ordered(uint32_t lo_bits, uint32_t hi_bits) {
-  uint32_t d;
-  asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi_bits)), "f"(__uint_as_float(lo_bits)));
-  return d;
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
