@@ -120,8 +120,9 @@ struct Bf16Layout {
   static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF_BYTES;
   // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], never, drain, c_loaded[EPI_WARPS],
-  // clc_full[kClcSlots], clc_empty[kClcSlots]
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 + EPI_WARPS + 2 * kClcSlots;
+  // clc_full[kClcSlots], clc_empty[kClcSlots], partner (two pairs per cluster: the second
+  // pair's partial sums are in the workspace)
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 + EPI_WARPS + 2 * kClcSlots + 1;
   static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // CLC responses, 16 bytes each
   // releases of a CLC response: producer B of each CTA, the MMA issuer, the epilogue warps
   // of each CTA, and for a pair producer A of the second CTA (the leader's issues them)
@@ -139,8 +140,11 @@ struct Bf16Layout {
 };
 
 // CLC: the instantiation with cluster launch control (p.clc == 1); the static one holds none
-// of its code.
-template <int CG, int STAGES, int ATOMS, int BN, bool SWAP, bool CLC>
+// of its code. PAIRS = 2 (swapped, two K splits): a cluster of two CTA pairs computes one
+// tile, each pair one half of K; the second pair writes its FP32 partial sums to the
+// workspace and signals the first pair's epilogue, which adds them before rounding. The
+// pairs of a cluster run at the same time, so no second kernel is needed.
+template <int CG, int STAGES, int ATOMS, int BN, bool SWAP, bool CLC, int PAIRS>
 __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                      const __grid_constant__ CUtensorMap tmap_b_half, const __grid_constant__ CUtensorMap tmap_c,
@@ -153,7 +157,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+  const uint32_t crank = (CG == 2) ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank & 1u;      // this CTA's place in its pair
+  const uint32_t leader = crank & ~1u;   // cluster rank of the pair's leader CTA
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << leader);
   const int cluster_idx = static_cast<int>(blockIdx.x) / CG;
   const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
@@ -166,7 +173,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
   const uint32_t bar_cload = bar_drain + 8;          // c_loaded[w]: epilogue warp w's prior-C tile landed
   const uint32_t bar_clc_full = bar_cload + 8 * L::EPI_WARPS;  // clc_full[s]: CLC response s landed here
   const uint32_t bar_clc_empty = bar_clc_full + 8 * kClcSlots; // clc_empty[s] (leader): response s released
-  const ClcRing ring{base + L::OFF_CLC, bar_clc_full, CG == 2 ? mapa_shared(bar_clc_empty, 0) : bar_clc_empty};
+  const uint32_t bar_partner = bar_clc_empty + 8 * kClcSlots;  // partner: the other pair's partial sums are written
+  const ClcRing ring{base + L::OFF_CLC, bar_clc_full, CG == 2 ? mapa_shared(bar_clc_empty, leader) : bar_clc_empty};
   constexpr bool clc = CLC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM_SLOT);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + L::OFF_ABORT);
@@ -188,6 +196,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       mbar_init(bar_clc_full + 8 * t, 1);
       mbar_init(bar_clc_empty + 8 * t, L::CLC_CONSUMERS);
     }
+    mbar_init(bar_partner, 32 * L::EPI_WARPS);
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
     // every response slot armed for its first use (re-armed by producer A as it reads them)
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           // The A producer arms the barrier with the stage's bytes (of both CTAs for a pair);
           // the B loads may complete before that arrival, the phase cannot.
           if (arm) mbar_arrive_expect_tx(full, (CG == 2 ? 2u : 1u) * stage_bytes);
-          const uint32_t target = CG == 2 ? mapa_shared(full, 0) : full;
+          const uint32_t target = CG == 2 ? mapa_shared(full, leader) : full;
           if (atoms == ATOMS) {
 #pragma unroll
             for (int a = 0; a < ATOMS; ++a) {
@@ -342,20 +351,20 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           }
           // Release the stage when these MMAs have read it; never wait here.
           if constexpr (CG == 1) mma_commit_local(bar_empty + 8 * stage);
-          else mma_commit_pair_multicast(bar_empty + 8 * stage, 0x3);
+          else mma_commit_pair_multicast(bar_empty + 8 * stage, pair_mask);
           stage = stage + 1 == STAGES ? 0u : stage + 1;
           phase = stage == 0 ? phase ^ 1u : phase;
         }
         if (!ok) break;
         if constexpr (CG == 1) mma_commit_local(bar_tfull + 8 * slot);
-        else mma_commit_pair_multicast(bar_tfull + 8 * slot, 0x3);
+        else mma_commit_pair_multicast(bar_tfull + 8 * slot, pair_mask);
         i = clc ? clc_next(ring, it, CG, false, true, wctx, status_code(kRoleMma, 0x300 + it % kClcSlots), ok)
                 : (i + num_clusters < p.num_items ? i + num_clusters : -1);
       }
       if (!ok) {
         // let issued MMAs finish before TMEM is released
         if constexpr (CG == 1) mma_commit_local(bar_drain);
-        else mma_commit_pair_multicast(bar_drain, 0x1);
+        else mma_commit_pair_multicast(bar_drain, static_cast<uint16_t>(1u << leader));
         wait_phase_slow(bar_drain, 0, wctx, status_code(kRoleMma, 0xFFFE), false);
         settle_after_abort();
       }
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     const uint32_t q = warp & 3u;  // this warp may access TMEM lanes 32q .. 32q+31
     const uint32_t epi = warp - 2u;
     const uint32_t stage_base = base + L::OFF_EPI + epi * L::EPI_BUFS * L::EPI_BUF_BYTES;
-    const uint32_t tempty_target = (CG == 2) ? mapa_shared(bar_tempty, 0) : bar_tempty;
+    const uint32_t tempty_target = (CG == 2) ? mapa_shared(bar_tempty, leader) : bar_tempty;
     const uint32_t cload = bar_cload + 8 * epi;
     uint32_t cload_phase = 0;
     bool epi_ok = true;
@@ -387,6 +396,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       }
       if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
       tc_fence_after_sync();
+      if constexpr (SWAP && PAIRS == 2) {
+        // the first pair waits until the second pair's partial sums are in the workspace
+        if (w.split == 0 && !wait_phase_warp(bar_partner, 0, wctx, status_code(kRoleEpilogue, 0x700))) break;
+      }
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * L::ACC_COLS;
       if (row0 < p.M) {
 #pragma unroll 1
@@ -397,7 +410,40 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           tmem_ld_32x32b_x32(taddr + c * 64, lo);
           tmem_ld_32x32b_x32(taddr + c * 64 + 32, hi);
           tmem_ld_wait();
-          if constexpr (SWAP) {
+          if constexpr (SWAP && PAIRS == 2) {
+            const int row = row0 + static_cast<int>(lane);
+            float* part = p.ws + static_cast<size_t>(row) * p.ldw + col;
+            if (w.split == 1) {
+              // the second pair: this row's 64 FP32 partial sums of the chunk to the workspace
+              if (row < p.M) {
+                float4* dst = reinterpret_cast<float4*>(part);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  dst[j] = make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
+                                       __uint_as_float(lo[4 * j + 2]), __uint_as_float(lo[4 * j + 3]));
+                  dst[8 + j] = make_float4(__uint_as_float(hi[4 * j]), __uint_as_float(hi[4 * j + 1]),
+                                           __uint_as_float(hi[4 * j + 2]), __uint_as_float(hi[4 * j + 3]));
+                }
+              }
+              continue;
+            }
+            // the first pair: add the second pair's partial sums (first half of K + second half)
+            if (row < p.M) {
+              const float4* src = reinterpret_cast<const float4*>(part);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 a = src[j], b = src[8 + j];
+                lo[4 * j] = __float_as_uint(__uint_as_float(lo[4 * j]) + a.x);
+                lo[4 * j + 1] = __float_as_uint(__uint_as_float(lo[4 * j + 1]) + a.y);
+                lo[4 * j + 2] = __float_as_uint(__uint_as_float(lo[4 * j + 2]) + a.z);
+                lo[4 * j + 3] = __float_as_uint(__uint_as_float(lo[4 * j + 3]) + a.w);
+                hi[4 * j] = __float_as_uint(__uint_as_float(hi[4 * j]) + b.x);
+                hi[4 * j + 1] = __float_as_uint(__uint_as_float(hi[4 * j + 1]) + b.y);
+                hi[4 * j + 2] = __float_as_uint(__uint_as_float(hi[4 * j + 2]) + b.z);
+                hi[4 * j + 3] = __float_as_uint(__uint_as_float(hi[4 * j + 3]) + b.w);
+              }
+            }
+          } else if constexpr (SWAP) {
             if (p.splits > 1) {
               // a K split: this row's 64 FP32 partial sums of the chunk to the workspace
               const int row = row0 + static_cast<int>(lane);
@@ -491,6 +537,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           }
           ebuf ^= 1u;
         }
+      }
+      if constexpr (SWAP && PAIRS == 2) {
+        // release this lane's partial sums to the first pair (same rows, cluster rank - 2)
+        if (w.split == 1) mbar_arrive_cluster(mapa_shared(bar_partner, crank - 2u));
       }
       if (!epi_ok) break;  // a prior-C load timed out (status recorded)
       // Accumulator slot drained: hand it back to the MMA issuer (leader CTA's barrier).
@@ -589,11 +639,13 @@ int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int split
   return GEMM_OK;
 }
 
-template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false>
+template <int CG, int STAGES, int ATOMS, int BN = 256, bool SWAP = false, int PAIRS = 1>
 struct Bf16Variant {
   using L = Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>;
-  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, false>;
-  static constexpr auto kernel_clc = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, true>;
+  static constexpr int CLUSTER = CG * PAIRS;  // CTAs per cluster
+  static constexpr auto kernel = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, false, PAIRS>;
+  // (two pairs per cluster never use CLC: the same instantiation stands in)
+  static constexpr auto kernel_clc = bf16_gemm_kernel<CG, STAGES, ATOMS, BN, SWAP, PAIRS == 1, PAIRS>;
 
   // Co-resident clusters per device, queried once per device.
   static int max_active_clusters(int device) {
@@ -607,11 +659,11 @@ struct Bf16Variant {
       return 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.gridDim = dim3(CG * 16, 1, 1);
+    cfg.gridDim = dim3(CLUSTER * 16, 1, 1);
     cfg.blockDim = dim3(L::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -688,14 +740,24 @@ struct Bf16Variant {
       const bool two_pay = BN == 64 && p.k_iters >= 48;
       if (splits < 2 || (splits == 2 && !two_pay)) splits = 1;
     }
+    if constexpr (SWAP && PAIRS == 1 && BN == 64 && CG == 2) {
+      // Two splits: one cluster of two pairs per tile adds the halves itself (no second
+      // kernel), when clusters of four CTAs can be launched.
+      if (splits == 2 && opt.clc != 1) {
+        using Two = Bf16Variant<CG, STAGES, ATOMS, BN, SWAP, 2>;
+        if (Two::max_active_clusters(device) > 0) return Two::run(A, B, C, M, N, K, stream, opt, device, info);
+      }
+    }
+    if constexpr (PAIRS == 2) splits = 2;
     p.k_per_split = ceil_div(p.k_iters, splits);
     p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split
     p.ldw = p.num_n_blocks * L::BLOCK_N;
     p.ws = nullptr;
     p.num_items = p.splits > 1 ? p.num_tiles * p.splits : p.num_tiles + p.split_tiles;
     // Cluster launch control: the whole grid of one cluster per item, taken dynamically
-    p.clc = (opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K, false)) ? 1 : 0;
-    const int clusters = p.clc ? p.num_items : std::min(p.num_items, wave);
+    p.clc = (PAIRS == 1 && opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K, false)) ? 1 : 0;
+    // (two pairs per cluster: every pair computes exactly one item)
+    const int clusters = (p.clc || PAIRS == 2) ? p.num_items : std::min(p.num_items, wave);
     p.wave = std::max(wave, 1);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
@@ -707,7 +769,7 @@ struct Bf16Variant {
     cfg.dynamicSmemBytes = L::SMEM_BYTES;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -718,7 +780,8 @@ struct Bf16Variant {
       // FP32 partials of every split, from the library's stream-ordered pool
       cudaMemPool_t pool = workspace_pool(device);
       void* ws = nullptr;
-      const size_t bytes = static_cast<size_t>(p.splits) * p.M * p.ldw * sizeof(float);
+      // (two pairs per cluster: only the second half of K goes through the workspace)
+      const size_t bytes = static_cast<size_t>(PAIRS == 2 ? 1 : p.splits) * p.M * p.ldw * sizeof(float);
       if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_OUT_OF_MEMORY;
@@ -734,7 +797,7 @@ struct Bf16Variant {
       count_launch();
     }
     if (p.splits > 1) {
-      if (st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream, opt.pdl);
+      if (PAIRS == 1 && st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream, opt.pdl);
       if (cudaFreeAsync(p.ws, stream) != cudaSuccess && st2 == GEMM_OK) st2 = GEMM_ERR_LAUNCH;
     }
     return st2;

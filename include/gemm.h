@@ -216,9 +216,11 @@ typedef struct {
     int no_split_k;      /* swapped BF16 GEMMs with at most half as many tiles as clusters:
                             0 = split K over 2 to 8 clusters per tile (at least 4 stages of
                             128 K each; two splits only for tile N 64 with at least 48 stages);
-                            each split writes FP32 partial sums to a workspace from the
-                            library's stream-ordered pool (as gemm_nvfp4's), and a second
-                            kernel adds them and rounds to BF16; 1 = never */
+                            the splits write FP32 partial sums to a workspace from the
+                            library's stream-ordered pool (as gemm_nvfp4's); a second kernel
+                            adds them and rounds to BF16, except for two splits, which run as
+                            one cluster of two CTA pairs per tile whose first pair adds the
+                            second pair's partials itself; 1 = never */
     int clc;             /* persistent grids (persistent = 1, max_clusters = 0): 0 = decided by
                             gemm_clc_rule; 1 = cluster launch control: one cluster per work item
                             is launched, and each running cluster takes the items of clusters it

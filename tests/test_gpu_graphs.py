@@ -36,8 +36,9 @@ def captured(fn, stream):
 
 
 @pytest.mark.parametrize("shape,clc", [((2304, 3072, 192), g.GEMM_CLC_OFF), ((2304, 3072, 192), g.GEMM_CLC_ON),
-                                       ((16, 1024, 8192), g.GEMM_CLC_AUTO), ((300, 264, 320), g.GEMM_CLC_AUTO)],
-                         ids=["static", "clc", "few_rows_split_k", "ragged"])
+                                       ((16, 1024, 8192), g.GEMM_CLC_AUTO), ((300, 264, 320), g.GEMM_CLC_AUTO),
+                                       ((8, 8192, 8192), g.GEMM_CLC_AUTO)],
+                         ids=["static", "clc", "few_rows_split_k", "ragged", "two_pairs_per_cluster"])
 def test_bf16_calls_replay_from_a_graph(shape, clc):
     M, N, K = shape
     A, B = si.bf16_problem(90, M, N, K, device=DEV)
