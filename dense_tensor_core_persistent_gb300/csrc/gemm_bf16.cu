@@ -140,10 +140,11 @@ struct Bf16Layout {
 };
 
 // CLC: the instantiation with cluster launch control (p.clc == 1); the static one holds none
-// of its code. PAIRS = 2 (swapped, two K splits): a cluster of two CTA pairs computes one
-// tile, each pair one half of K; the second pair writes its FP32 partial sums to the
-// workspace and signals the first pair's epilogue, which adds them before rounding. The
-// pairs of a cluster run at the same time, so no second kernel is needed.
+// of its code. PAIRS = 2 or 4 (swapped, that many K splits): a cluster of PAIRS CTA pairs
+// computes one tile, pair s the s-th part of K; pairs 1 .. PAIRS-1 write their FP32 partial
+// sums to the workspace and signal the first pair's epilogue, which adds them (in split
+// order) before rounding. The pairs of a cluster run at the same time, so no second kernel
+// is needed.
 template <int CG, int STAGES, int ATOMS, int BN, bool SWAP, bool CLC, int PAIRS>
 __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_THREADS, 1)
     bf16_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
@@ -196,7 +197,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       mbar_init(bar_clc_full + 8 * t, 1);
       mbar_init(bar_clc_empty + 8 * t, L::CLC_CONSUMERS);
     }
-    mbar_init(bar_partner, 32 * L::EPI_WARPS);
+    mbar_init(bar_partner, PAIRS > 1 ? 32 * L::EPI_WARPS * (PAIRS - 1) : 1);
     *abort_flag = 0u;
     fence_mbarrier_init_cluster();
     // every response slot armed for its first use (re-armed by producer A as it reads them)
@@ -396,8 +397,8 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
       }
       if (!wait_phase_warp(bar_tfull + 8 * slot, acc_phase, wctx, status_code(kRoleEpilogue, slot))) break;
       tc_fence_after_sync();
-      if constexpr (SWAP && PAIRS == 2) {
-        // the first pair waits until the second pair's partial sums are in the workspace
+      if constexpr (SWAP && PAIRS > 1) {
+        // the first pair waits until the other pairs' partial sums are in the workspace
         if (w.split == 0 && !wait_phase_warp(bar_partner, 0, wctx, status_code(kRoleEpilogue, 0x700))) break;
       }
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + slot * L::ACC_COLS;
@@ -410,13 +411,13 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           tmem_ld_32x32b_x32(taddr + c * 64, lo);
           tmem_ld_32x32b_x32(taddr + c * 64 + 32, hi);
           tmem_ld_wait();
-          if constexpr (SWAP && PAIRS == 2) {
+          if constexpr (SWAP && PAIRS > 1) {
             const int row = row0 + static_cast<int>(lane);
-            float* part = p.ws + static_cast<size_t>(row) * p.ldw + col;
-            if (w.split == 1) {
-              // the second pair: this row's 64 FP32 partial sums of the chunk to the workspace
+            if (w.split >= 1) {
+              // pair s >= 1: this row's 64 FP32 partial sums of the chunk to workspace slot s - 1
               if (row < p.M) {
-                float4* dst = reinterpret_cast<float4*>(part);
+                float4* dst = reinterpret_cast<float4*>(
+                    p.ws + (static_cast<size_t>(w.split - 1) * p.M + row) * p.ldw + col);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                   dst[j] = make_float4(__uint_as_float(lo[4 * j]), __uint_as_float(lo[4 * j + 1]),
@@ -427,12 +428,15 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
               }
               continue;
             }
-            // the first pair: add the second pair's partial sums (first half of K + second half)
+            // the first pair: add the other pairs' partial sums, in split order
             if (row < p.M) {
-              const float4* src = reinterpret_cast<const float4*>(part);
+#pragma unroll 1
+              for (int sp = 0; sp < PAIRS - 1; ++sp) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    p.ws + (static_cast<size_t>(sp) * p.M + row) * p.ldw + col);
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 a = src[j], b = src[8 + j];
+                for (int j = 0; j < 8; ++j) {
+                  const float4 a = src[j], b = src[8 + j];
                 lo[4 * j] = __float_as_uint(__uint_as_float(lo[4 * j]) + a.x);
                 lo[4 * j + 1] = __float_as_uint(__uint_as_float(lo[4 * j + 1]) + a.y);
                 lo[4 * j + 2] = __float_as_uint(__uint_as_float(lo[4 * j + 2]) + a.z);
@@ -441,6 +445,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
                 hi[4 * j + 1] = __float_as_uint(__uint_as_float(hi[4 * j + 1]) + b.y);
                 hi[4 * j + 2] = __float_as_uint(__uint_as_float(hi[4 * j + 2]) + b.z);
                 hi[4 * j + 3] = __float_as_uint(__uint_as_float(hi[4 * j + 3]) + b.w);
+                }
               }
             }
           } else if constexpr (SWAP) {
@@ -538,9 +543,10 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           ebuf ^= 1u;
         }
       }
-      if constexpr (SWAP && PAIRS == 2) {
-        // release this lane's partial sums to the first pair (same rows, cluster rank - 2)
-        if (w.split == 1) mbar_arrive_cluster(mapa_shared(bar_partner, crank - 2u));
+      if constexpr (SWAP && PAIRS > 1) {
+        // release this lane's partial sums to the first pair's CTA that holds the same rows
+        // (cluster rank 0 or 1: this CTA's place in its pair)
+        if (w.split >= 1) mbar_arrive_cluster(mapa_shared(bar_partner, rank));
       }
       if (!epi_ok) break;  // a prior-C load timed out (status recorded)
       // Accumulator slot drained: hand it back to the MMA issuer (leader CTA's barrier).
@@ -740,24 +746,27 @@ struct Bf16Variant {
       const bool two_pay = BN == 64 && p.k_iters >= 48;
       if (splits < 2 || (splits == 2 && !two_pay)) splits = 1;
     }
-    if constexpr (SWAP && PAIRS == 1 && BN == 64 && CG == 2) {
+    if constexpr (SWAP && PAIRS == 1 && CG == 2 && BN == 64) {
       // Two splits: one cluster of two pairs per tile adds the halves itself (no second
-      // kernel), when clusters of four CTAs can be launched.
-      if (splits == 2 && opt.clc != 1) {
+      // kernel), when enough clusters of four CTAs fit for all tiles at once. (Four pairs
+      // per cluster for four splits measured slower than the reduction kernel: 18.1 against
+      // 12.8 us at M = 100, N = K = 2048.)
+      if (opt.clc != 1 && opt.max_clusters == 0 && splits == 2) {
         using Two = Bf16Variant<CG, STAGES, ATOMS, BN, SWAP, 2>;
-        if (Two::max_active_clusters(device) > 0) return Two::run(A, B, C, M, N, K, stream, opt, device, info);
+        if (Two::max_active_clusters(device) >= p.num_tiles) return Two::run(A, B, C, M, N, K, stream, opt, device, info);
       }
     }
-    if constexpr (PAIRS == 2) splits = 2;
+    if constexpr (PAIRS > 1) splits = PAIRS;
     p.k_per_split = ceil_div(p.k_iters, splits);
     p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split
+    if (PAIRS > 1 && p.splits != PAIRS) return GEMM_ERR_UNSUPPORTED_SHAPE;  // (the split rule rules it out)
     p.ldw = p.num_n_blocks * L::BLOCK_N;
     p.ws = nullptr;
     p.num_items = p.splits > 1 ? p.num_tiles * p.splits : p.num_tiles + p.split_tiles;
     // Cluster launch control: the whole grid of one cluster per item, taken dynamically
     p.clc = (PAIRS == 1 && opt.persistent && opt.max_clusters == 0 && use_clc(opt.clc, p.num_items, max_clusters, K, false)) ? 1 : 0;
     // (two pairs per cluster: every pair computes exactly one item)
-    const int clusters = (p.clc || PAIRS == 2) ? p.num_items : std::min(p.num_items, wave);
+    const int clusters = (p.clc || PAIRS > 1) ? p.num_items : std::min(p.num_items, wave);
     p.wave = std::max(wave, 1);
     p.group_m = opt.group_m > 0 ? std::min(opt.group_m, p.num_m_blocks)
                                 : choose_group_m(M, N, K, L::TILE_M, L::BLOCK_N, 2.0, 0.0, clusters, info.l2_bytes);
@@ -780,8 +789,8 @@ struct Bf16Variant {
       // FP32 partials of every split, from the library's stream-ordered pool
       cudaMemPool_t pool = workspace_pool(device);
       void* ws = nullptr;
-      // (two pairs per cluster: only the second half of K goes through the workspace)
-      const size_t bytes = static_cast<size_t>(PAIRS == 2 ? 1 : p.splits) * p.M * p.ldw * sizeof(float);
+      // (several pairs per cluster: the first pair's part never goes through the workspace)
+      const size_t bytes = static_cast<size_t>(PAIRS > 1 ? PAIRS - 1 : p.splits) * p.M * p.ldw * sizeof(float);
       if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes, pool, stream) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_OUT_OF_MEMORY;
