@@ -474,8 +474,38 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
           uint32_t pk[32];
           if constexpr (SWAP) {
             // columns i and 32 + i of this lane's accumulator row, for the transposed tile
+            if (!p.epi.fused) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2_rn(lo[i], hi[i]);
+              for (int i = 0; i < 32; ++i) pk[i] = pack_bf16x2_rn(lo[i], hi[i]);
+            } else {
+              // fused epilogue: this lane is column n = row0 + lane of the caller's C, so its
+              // bias is one value; its prior C is column `lane` of the transposed 64 x 32 tile
+              // (TMA-loaded into the staging buffer, zeros past the caller's M and N)
+              const int n = row0 + static_cast<int>(lane);
+              const uint32_t bv = (p.epi.bias != nullptr && n < p.M) ? static_cast<uint32_t>(p.epi.bias[n]) : 0u;
+              const uint32_t bias2 = bv | (bv << 16);
+              const bool with_old = p.epi.beta != 0.0f;
+              if (with_old) {
+                if (lane == 0) {
+                  mbar_arrive_expect_tx(cload, L::EPI_BUF_BYTES);
+                  tma_load_2d(buf, &tmap_c, row0, col, cload);  // (column, row) of the caller's C
+                }
+                if (!wait_phase_warp(cload, cload_phase, wctx, status_code(kRoleEpilogue, 2))) {
+                  epi_ok = false;
+                  break;
+                }
+                cload_phase ^= 1u;
+              }
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const uint32_t old2 = with_old ? (ld_shared_u16(buf + i * 64 + lane * 2) |
+                                                  (ld_shared_u16(buf + (32 + i) * 64 + lane * 2) << 16))
+                                               : 0u;
+                pk[i] = epi_pair(lo[i], hi[i], old2, bias2, p.epi);
+              }
+              // every lane has read its column of the prior C before any lane overwrites it
+              __syncwarp();
+            }
           } else if (!p.epi.fused) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -757,6 +787,9 @@ struct Bf16Variant {
       }
     }
     if constexpr (PAIRS > 1) splits = PAIRS;
+    // the reduction kernel applies no fused epilogue: fused calls keep one split there (two
+    // pairs per cluster apply it in the first pair, after adding the second pair's partials)
+    if (PAIRS == 1 && p.epi.fused) splits = 1;
     p.k_per_split = ceil_div(p.k_iters, splits);
     p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split
     if (PAIRS > 1 && p.splits != PAIRS) return GEMM_ERR_UNSUPPORTED_SHAPE;  // (the split rule rules it out)
@@ -825,7 +858,7 @@ using Bf16Swap128 = Bf16Variant<2, 4, 2, 128, true>;
 // A GEMM with few rows wastes most of each M = 256 MMA on padding; computed as C^T = B A^T
 // its rows become the MMA's N (64 or 128) and the long N dimension fills the 256 MMA rows.
 bool bf16_swap_ab(int M, int N, const RunOptions& opt) {
-  return opt.swap_ab && opt.kernel == GEMM_KERNEL_DEFAULT && !opt.epi.fused() && M >= 1 && M <= 128 && N >= 256;
+  return opt.swap_ab && opt.kernel == GEMM_KERNEL_DEFAULT && M >= 1 && M <= 128 && N >= 256;
 }
 
 int bf16_tile_n(int M, int N, const RunOptions& opt) {

@@ -75,8 +75,9 @@ typedef enum {
  * a 256 x 256 output tile per CTA pair, double-buffered TMEM accumulator and a
  * TMA-store epilogue; one kernel launch per call. With M <= 128 and N >= 256 it
  * computes C^T = B A^T instead (tile N 64 or 128; see gemm_options_t.no_swap_ab), and
- * such a GEMM with few tiles splits K: a second launch adds the FP32 partial sums
- * (workspace from the library's stream-ordered pool, as for gemm_nvfp4; see no_split_k).
+ * such a GEMM with few tiles splits K: the FP32 partial sums are added by a second launch
+ * or, for two splits, inside the one launch (workspace from the library's stream-ordered
+ * pool, as for gemm_nvfp4; see no_split_k).
  */
 int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* stream);
 
@@ -209,7 +210,7 @@ typedef struct {
     int no_pdl;          /* 0: launch with programmatic stream serialization (the kernel's
                             set-up overlaps the end of the previous kernel on the stream;
                             every global access waits for that kernel); 1: plain launch */
-    int no_swap_ab;      /* BF16, default kernel, no fused epilogue: 0 = a GEMM with M <= 128
+    int no_swap_ab;      /* BF16, default kernel (fused epilogue or not): 0 = a GEMM with M <= 128
                             and N >= 256 computes C^T = B A^T, so that the few rows of A fill
                             the MMA's N dimension (64 or 128) instead of padding its 256 rows,
                             and its epilogue writes C transposed; 1 = never */
@@ -220,7 +221,8 @@ typedef struct {
                             library's stream-ordered pool (as gemm_nvfp4's); a second kernel
                             adds them and rounds to BF16, except for two splits, which run as
                             one cluster of two CTA pairs per tile whose first pair adds the
-                            second pair's partials itself; 1 = never */
+                            second pair's partials itself (with a fused epilogue only two
+                            splits are used); 1 = never */
     int clc;             /* persistent grids (persistent = 1, max_clusters = 0): 0 = decided by
                             gemm_clc_rule; 1 = cluster launch control: one cluster per work item
                             is launched, and each running cluster takes the items of clusters it

@@ -120,7 +120,7 @@ def test_mma_rate_argument_errors():
 
 
 def test_bf16_plan_swaps_few_row_gemms():
-    """C^T = B A^T for M <= 128 and N >= 256 on the default kernel without a fused epilogue."""
+    """C^T = B A^T for M <= 128 and N >= 256 on the default kernel, with or without a fused epilogue."""
     assert g.bf16_plan(16, 8192, 8192) == (1, 64)
     assert g.bf16_plan(1, 256, 64) == (1, 64)
     assert g.bf16_plan(64, 8192, 8192) == (1, 64)
@@ -131,7 +131,7 @@ def test_bf16_plan_swaps_few_row_gemms():
     assert g.bf16_plan(16, 8192, 8192, g.options(no_swap_ab=1)) == (0, 256)
     assert g.bf16_plan(16, 8192, 8192, g.options(kernel=g.GEMM_KERNEL_BF16_2CTA)) == (0, 256)
     assert g.bf16_plan(16, 8192, 8192, g.options(kernel=g.GEMM_KERNEL_BF16_1CTA)) == (0, 256)
-    assert g.bf16_plan(16, 8192, 8192, epi=g.epilogue(activation=g.GEMM_ACT_RELU)) == (0, 256)
+    assert g.bf16_plan(16, 8192, 8192, epi=g.epilogue(activation=g.GEMM_ACT_RELU)) == (1, 64)  # fused, swapped
     assert g.bf16_plan(16, 8192, 8192, epi=g.epilogue()) == (1, 64)   # the identity epilogue is not fused
     with pytest.raises(g.GemmError):
         g.bf16_plan(-1, 8, 8)

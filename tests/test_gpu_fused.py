@@ -271,3 +271,45 @@ def test_beta_reads_the_previous_result_on_one_stream(kind, no_pdl):
         s.synchronize()
         ref = oracle.epilogue(oracle.gemm_nvfp4(*[t.cpu() for t in p2]), 1.0, 1.0, bits(first_c), None)
         assert_nvfp4_close(bits(C), ref, "chained")
+
+
+# ---------------------------------------------------------------- few rows: swapped (C^T = B A^T)
+
+FEW_ROW_SHAPES = [
+    (1, 1024, 512),      # tile N 64
+    (16, 2056, 1024),    # ragged N
+    (64, 520, 1024),     # ragged last block of the long dimension
+    (100, 776, 136),     # tile N 128, partial K stage
+    (16, 1024, 4096),    # would split K 8 ways; a fused call keeps one split
+    (4, 8192, 6144),     # two splits: one cluster of two pairs, the first applies the epilogue
+]
+
+
+@pytest.mark.parametrize("variant", sorted(VARIANTS))
+@pytest.mark.parametrize("shape", FEW_ROW_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bf16_fused_few_rows_swapped(variant, shape):
+    M, N, K = shape
+    assert g.bf16_plan(M, N, K, epi=g.epilogue(activation=g.GEMM_ACT_RELU))[0] == 1
+    A, B = si.bf16_problem(M + N + K, M, N, K)
+    alpha, beta, bias, act = epilogue_args(variant, N, 40)
+    c_old = prior_c(M, N, 41)
+    got = run_bf16_fused(A, B, c_old, alpha, beta, bias, act)
+    assert_fused_close(got, oracle.gemm_bf16(A, B), alpha, beta, c_old, bias, act, K, f"{variant} {shape}")
+    # the same call without swap-AB agrees within the same tolerance
+    got2 = run_bf16_fused(A, B, c_old, alpha, beta, bias, act, opts=g.options(no_swap_ab=1))
+    assert_fused_close(got2, oracle.gemm_bf16(A, B), alpha, beta, c_old, bias, act, K, f"{variant} {shape} no swap")
+
+
+def test_bf16_fused_few_rows_integer_inputs_bit_exact():
+    # integer operands, power-of-two alpha and beta, integer bias: every step exact in FP32
+    M, N, K = 48, 2048, 256
+    A, B = si.bf16_problem(42, M, N, K, kind="int")
+    bias = np.arange(N, dtype=np.float32) % 7 - 3
+    bias = torch.from_numpy(bias).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    c_old = prior_c(M, N, 43)
+    c_old_int = torch.from_numpy(np.round(oracle.bf16_bits_to_f64(c_old) * 4)).to(torch.bfloat16)
+    c_old = c_old_int.view(torch.int16).numpy().view(np.uint16)
+    got = run_bf16_fused(A, B, c_old, 2.0, 0.5, bias, g.GEMM_ACT_RELU)
+    want = oracle.round_bf16(oracle.epilogue(oracle.gemm_bf16(A, B), 2.0, 0.5, c_old, bias, g.GEMM_ACT_RELU))
+    assert np.array_equal(oracle.bf16_bits_to_f64(got), oracle.bf16_bits_to_f64(want))
+
