@@ -626,7 +626,7 @@ namespace {
 constexpr int kMaxSplits = 8;
 
 __global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __restrict__ ws, uint16_t* __restrict__ C,
-                                                                int rows, int cols, int splits, int ldw) {
+                                                                int rows, int cols, int splits, int ldw, EpiParams epi) {
   __shared__ float t[32][33];
   pdl_launch_dependents();
   pdl_wait();
@@ -651,12 +651,22 @@ __global__ void __launch_bounds__(256) splitk_reduce_transposed(const float* __r
   __syncthreads();
   for (int r = threadIdx.y; r < 32; r += 8) {
     const int mm = m0 + r, n = n0 + static_cast<int>(threadIdx.x);
-    if (mm < rows && n < cols) C[static_cast<size_t>(mm) * cols + n] = __bfloat16_as_ushort(__float2bfloat16_rn(t[threadIdx.x][r]));
+    if (mm < rows && n < cols) {
+      uint16_t* c = C + static_cast<size_t>(mm) * cols + n;
+      if (!epi.fused) {
+        *c = __bfloat16_as_ushort(__float2bfloat16_rn(t[threadIdx.x][r]));
+      } else {
+        // the fused epilogue on one value: the pair arithmetic of the GEMM epilogues, low half
+        const uint32_t old = epi.beta != 0.0f ? static_cast<uint32_t>(*c) : 0u;
+        const uint32_t bias = epi.bias != nullptr ? static_cast<uint32_t>(epi.bias[n]) : 0u;
+        *c = static_cast<uint16_t>(epi_pair(__float_as_uint(t[threadIdx.x][r]), 0u, old, bias, epi) & 0xFFFFu);
+      }
+    }
   }
 }
 
-int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int splits, int ldw, cudaStream_t stream,
-                         int pdl) {
+int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int splits, int ldw, const EpiParams& epi,
+                         cudaStream_t stream, int pdl) {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(cols, 32)), static_cast<unsigned>(ceil_div(rows, 32)), 1);
@@ -666,7 +676,7 @@ int launch_splitk_reduce(const float* ws, void* C, int rows, int cols, int split
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, splitk_reduce_transposed, ws, static_cast<uint16_t*>(C), rows, cols, splits, ldw) !=
+  if (cudaLaunchKernelEx(&cfg, splitk_reduce_transposed, ws, static_cast<uint16_t*>(C), rows, cols, splits, ldw, epi) !=
       cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_LAUNCH;
@@ -787,9 +797,6 @@ struct Bf16Variant {
       }
     }
     if constexpr (PAIRS > 1) splits = PAIRS;
-    // the reduction kernel applies no fused epilogue: fused calls keep one split there (two
-    // pairs per cluster apply it in the first pair, after adding the second pair's partials)
-    if (PAIRS == 1 && p.epi.fused) splits = 1;
     p.k_per_split = ceil_div(p.k_iters, splits);
     p.splits = ceil_div(p.k_iters, p.k_per_split);  // no empty split
     if (PAIRS > 1 && p.splits != PAIRS) return GEMM_ERR_UNSUPPORTED_SHAPE;  // (the split rule rules it out)
@@ -839,7 +846,8 @@ struct Bf16Variant {
       count_launch();
     }
     if (p.splits > 1) {
-      if (PAIRS == 1 && st2 == GEMM_OK) st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, stream, opt.pdl);
+      if (PAIRS == 1 && st2 == GEMM_OK)
+        st2 = launch_splitk_reduce(p.ws, C, p.N, p.M, p.splits, p.ldw, p.epi, stream, opt.pdl);
       if (cudaFreeAsync(p.ws, stream) != cudaSuccess && st2 == GEMM_OK) st2 = GEMM_ERR_LAUNCH;
     }
     return st2;

@@ -221,8 +221,8 @@ typedef struct {
                             library's stream-ordered pool (as gemm_nvfp4's); a second kernel
                             adds them and rounds to BF16, except for two splits, which run as
                             one cluster of two CTA pairs per tile whose first pair adds the
-                            second pair's partials itself (with a fused epilogue only two
-                            splits are used); 1 = never */
+                            second pair's partials itself; with a fused epilogue, the kernel
+                            that adds the partials applies it; 1 = never */
     int clc;             /* persistent grids (persistent = 1, max_clusters = 0): 0 = decided by
                             gemm_clc_rule; 1 = cluster launch control: one cluster per work item
                             is launched, and each running cluster takes the items of clusters it

@@ -280,7 +280,7 @@ FEW_ROW_SHAPES = [
     (16, 2056, 1024),    # ragged N
     (64, 520, 1024),     # ragged last block of the long dimension
     (100, 776, 136),     # tile N 128, partial K stage
-    (16, 1024, 4096),    # would split K 8 ways; a fused call keeps one split
+    (16, 1024, 4096),    # K split 8 ways: the reduction kernel applies the epilogue
     (4, 8192, 6144),     # two splits: one cluster of two pairs, the first applies the epilogue
 ]
 
