@@ -312,11 +312,12 @@ int gemm_tile_coord(int M, int N, int tile_m, int tile_n, int group_m, int t, in
 
 /*
  * gemm_choose_group_m -- the group size the library picks for a problem when
- * options->group_m is 0. Balances the bytes of A and B that the co-resident
- * tiles of one wave touch, and shrinks the group until that wave footprint
- * fits in the L2 cache ("NVFP4 GEMM on Blackwell", Production Kernel,
- * "Supergroup Size", with the roles of M and N exchanged because the groups
- * here run along M). elem_bytes_x2 is twice the bytes per operand element
+ * options->group_m is 0. Balances the bytes of A and B that the tiles of two
+ * waves of co-resident clusters (concurrent_tiles each) touch, and shrinks the
+ * group until that footprint fits in the L2 cache ("NVFP4 GEMM on Blackwell",
+ * Production Kernel, "Supergroup Size", with the roles of M and N exchanged
+ * because the groups here run along M). Two waves: each wave starts on the K
+ * blocks the previous one read last, so their operands share L2. elem_bytes_x2 is twice the bytes per operand element
  * (4 for BF16, 1 for packed E2M1 plus the scale bytes counted separately:
  * pass 1 and the function adds K/16 scale bytes per row).
  */

@@ -104,11 +104,13 @@ def test_group_choice():
     L2 = 126 * 2 ** 20
     # operands fit in L2: walk all of M
     assert g.choose_group_m(4096, 4096, 4096, 256, 256, 4, 74, L2) == 16
-    # 8192^3 BF16: balanced wave sqrt(74) ~ 9 M-blocks
-    assert g.choose_group_m(8192, 8192, 8192, 256, 256, 4, 74, L2) == 9
-    # a very large K shrinks the group until a wave's operands fit
-    gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 74, L2)
-    assert 1 <= gl < 9
+    # 8192^3 BF16, 76 co-resident pairs: two waves balanced at sqrt(2 * 76) ~ 12 M-blocks
+    assert g.choose_group_m(8192, 8192, 8192, 256, 256, 4, 76, L2) == 12
+    assert g.choose_group_m(6144, 6144, 6144, 256, 256, 4, 76, L2) == 12
+    assert g.choose_group_m(4000, 14336, 4096, 256, 256, 4, 76, L2) == 12
+    # a very large K shrinks the group until two waves' operands fit
+    gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 76, L2)
+    assert 1 <= gl < 12
     assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 74, L2) >= 1
 
 
