@@ -108,6 +108,10 @@ def test_group_choice():
     assert g.choose_group_m(8192, 8192, 8192, 256, 256, 4, 76, L2) == 12
     assert g.choose_group_m(6144, 6144, 6144, 256, 256, 4, 76, L2) == 12
     assert g.choose_group_m(4000, 14336, 4096, 256, 256, 4, 76, L2) == 12
+    # NVFP4 (half a byte per element plus a scale byte per 16): operands that fit in L2 walk all
+    # of M; larger ones balance two waves like BF16
+    assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 76, L2) == 32
+    assert g.choose_group_m(16384, 16384, 16384, 256, 256, 1, 76, L2) == 12
     # a very large K shrinks the group until two waves' operands fit
     gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 76, L2)
     assert 1 <= gl < 12
