@@ -23,7 +23,8 @@ struct TileCoord {
   int n_blk;
 };
 
-DTCP_HD int ceil_div(int a, int b) { return (a + b - 1) / b; }
+// a >= 0, b > 0; no intermediate exceeds a, so a near INT_MAX does not overflow.
+DTCP_HD int ceil_div(int a, int b) { return a / b + (a % b != 0 ? 1 : 0); }
 
 // Tile index t (0 <= t < num_m * num_n) -> block coordinates. Requires 1 <= group_m.
 DTCP_HD TileCoord tile_coord(int t, int num_m, int num_n, int group_m) {

@@ -49,6 +49,12 @@ def test_argument_errors_are_reported_before_any_device_use():
     assert l.gemm_bf16(16, 24, 8, 8, 8, 8, 0) == g.GEMM_ERR_MISALIGNED
     assert l.gemm_nvfp4(16, 16, 16, 16, 16, 8, 8, 128, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE  # K % 256
     assert l.gemm_nvfp4(16, 16, 16, 0, 16, 8, 8, 256, 0) == g.GEMM_ERR_INVALID_ARG
+    # sizes near INT_MAX: the row-block counts are far beyond what a launch can hold, and
+    # their computation must not overflow into a negative count that passes the check
+    big = 2**31 - 1
+    assert l.gemm_nvfp4(16, 16, 16, 16, 16, big, 8, 256, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE
+    assert l.gemm_nvfp4(16, 16, 16, 16, 16, 8, big - 7, 256, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE
+    assert l.gemm_nvfp4_noalloc(16, 16, 16, 16, 16, big, 8, 256, 0) == g.GEMM_ERR_UNSUPPORTED_SHAPE
     o = g.options()
     o.clc = 3
     with pytest.raises(g.GemmError):

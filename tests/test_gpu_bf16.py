@@ -174,16 +174,37 @@ def _full_size_sampled(seed, M, N, K, kind="uniform", n=4096, exact=False):
         assert_bf16_close(got, ref, K, f"{M}x{N}x{K}")
 
 
-def test_c2_4096_cubed_sampled():
-    _full_size_sampled(1, 4096, 4096, 4096)
+def _full_size_every_element(seed, M, N, K, kind="uniform", exact=False, block=2048):
+    """A configuration at its full size, in the launch the benchmark times, compared with the
+    oracle on every output (the oracle runs on blocks of `block` rows)."""
+    A, B = si.bf16_problem(seed, M, N, K, kind=kind, device=DEV)
+    C = g.matmul_bf16(A, B)
+    torch.cuda.synchronize()
+    got = bits(C)
+    Ah, Bh = A.cpu(), B.cpu()
+    for r0 in range(0, M, block):
+        r1 = min(M, r0 + block)
+        ref = oracle.gemm_bf16(Ah, Bh, r0, r1)
+        if exact:
+            assert_bf16_exact(got[r0:r1], ref, f"{M}x{N}x{K} {kind} rows {r0}..")
+        else:
+            assert_bf16_close(got[r0:r1], ref, K, f"{M}x{N}x{K} rows {r0}..")
+
+
+def test_c2_4096_cubed_every_element():
+    """4096^3 from seed 1: all 16.8M outputs (about 3 s of oracle time)."""
+    _full_size_every_element(1, 4096, 4096, 4096)
 
 
 def test_c3_8192_cubed_sampled():
     _full_size_sampled(2, 8192, 8192, 8192)
 
 
-def test_c4_ragged_4000x14336x4096_sampled():
-    _full_size_sampled(3, 4000, 14336, 4096)
+def test_c4_ragged_4000x14336x4096_every_element():
+    """4000 x 14336 x 4096 from seed 3: all 57.3M outputs, including the last row block, whose
+    second CTA holds rows 3968..3999 and reads zeros (TMA out-of-bounds fill) past row 3999.
+    Blocks of 1000 rows put a block boundary inside that last 256-row tile."""
+    _full_size_every_element(3, 4000, 14336, 4096, block=1000)
 
 
 @pytest.mark.parametrize("shape", [(64, 28672, 8192), (1, 8192, 8192), (128, 8192, 8192)],
@@ -196,9 +217,11 @@ def test_few_rows_full_size_sampled(shape):
     _full_size_sampled(11, M, N, K, n=min(4096, M * N))
 
 
-def test_c3_shape_integer_inputs_sampled_bit_exact():
-    # |partial sums| <= 16 * 8192 < 2^24: exact in FP32 at the full size
-    _full_size_sampled(2, 8192, 8192, 8192, kind="int", n=8192, exact=True)
+@pytest.mark.slow
+def test_c3_shape_integer_inputs_every_element_bit_exact():
+    """The 8192^3 shape with integers in [-4, 4] from seed 2: |partial sums| <= 16 * 8192 <
+    2^24, so every FP32 sum is exact and all 67M outputs must equal the oracle's rounding."""
+    _full_size_every_element(2, 8192, 8192, 8192, kind="int", exact=True)
 
 
 def test_generator_same_values_on_gpu_and_cpu():

@@ -261,13 +261,16 @@ def test_back_to_back_calls_on_one_stream(no_pdl):
 
 @pytest.mark.slow
 def test_c5_8192_cubed_every_element():
-    """C5 in the launch the benchmark times (blocked scales), compared with the oracle on all
-    67M outputs, in 2048-row blocks."""
+    """C5 in the launch the benchmark times (gemm_nvfp4 on row-major scales, packed inside
+    the call), compared with the oracle on all 67M outputs, in 2048-row blocks. The same
+    operands through gemm_nvfp4_blocked must give the identical bits (one GEMM kernel)."""
     M = N = K = 8192
     a, sfa, b, sfb = si.nvfp4_problem(4, M, N, K, device=DEV)
-    C = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb))
+    C = g.matmul_nvfp4(a, sfa, b, sfb)
+    Cb = g.matmul_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb))
     torch.cuda.synchronize()
     got = bits(C)
+    assert np.array_equal(got, bits(Cb))
     ah, sah, bh, sbh = a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu()
     for r0 in range(0, M, 2048):
         assert_nvfp4_close(got[r0:r0 + 2048], oracle.gemm_nvfp4(ah, sah, bh, sbh, r0, r0 + 2048), f"C5 rows {r0}..")
