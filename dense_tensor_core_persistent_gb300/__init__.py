@@ -311,6 +311,12 @@ def launch_count() -> int:
 
 GEMM_MMA_BF16 = 0
 GEMM_MMA_NVFP4 = 1
+GEMM_MMA_NVFP4_1CTA_N128 = 2
+GEMM_MMA_NVFP4_1CTA_N192 = 3
+GEMM_MMA_NVFP4_1CTA_N256 = 4
+GEMM_MMA_NVFP4_PAIR_N128 = 5
+GEMM_MMA_NVFP4_PAIR_N128_2ACC = 6
+GEMM_MMA_MXF4_PAIR_N256 = 7
 
 
 def measure_mma_rate(kind: int) -> float:

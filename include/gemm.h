@@ -338,21 +338,35 @@ int gemm_bf16_plan(int M, int N, int K, const gemm_options_t* options, const gem
 unsigned long long gemm_launch_count(void);
 
 /*
- * gemm_measure_mma_rate -- measures, on the current device, the throughput of one of the
- * two tensor-core MMA kinds the GEMMs issue, as FLOP per SM clock: one CTA pair per two
- * SMs issues 8192 back-to-back M = 256, N = 256 MMAs (cta_group::2) into one TMEM
- * accumulator from shared memory, timed with the SM clock (the second of two launches).
- *   kind: GEMM_MMA_BF16  -- kind::f16, BF16 operands, K = 16 per instruction;
+ * gemm_measure_mma_rate -- measures, on the current device, the throughput of one
+ * tensor-core MMA instruction form as FLOP per SM clock: one issuing thread per CTA pair
+ * (cta_group::2, M = 256) or per CTA (cta_group::1, M = 128) issues 8192 back-to-back
+ * MMAs from shared memory into TMEM, timed with the SM clock (the second of two launches).
+ *   kind: GEMM_MMA_BF16  -- kind::f16, BF16 operands, K = 16, M = 256, N = 256 (the BF16 GEMM);
  *         GEMM_MMA_NVFP4 -- kind::mxf4nvf4.block_scale.scale_vec::4X, E2M1 operands with
- *                           UE4M3 scales, K = 64 per instruction.
- *   *flop_per_clock_per_sm: the result (2 * M * N * K per instruction, per SM, per clock).
+ *                           UE4M3 scales per 16 elements, K = 64, M = 256, N = 256 (the NVFP4 GEMM);
+ *         GEMM_MMA_NVFP4_1CTA_N128 / _N192 / _N256 -- the same kind at M = 128 (cta_group::1);
+ *         GEMM_MMA_NVFP4_PAIR_N128 -- M = 256, N = 128, one accumulator;
+ *         GEMM_MMA_NVFP4_PAIR_N128_2ACC -- M = 256, N = 128, alternating between two accumulators;
+ *         GEMM_MMA_MXF4_PAIR_N256 -- kind::mxf4.block_scale.scale_vec::2X (UE8M0 scales per 32
+ *                           elements), K = 64, M = 256, N = 256.
+ *   *flop_per_clock_per_sm: the result (2 * 128 * N * K per instruction and SM, per clock).
  * It is the ceiling a kernel made of these instructions can reach per clock; multiplied
  * by the SM count and clock it gives TFLOP/s. Synchronous: it runs on a private stream
  * and waits for it. Device memory: none beyond the library's static device arrays.
  * Errors: GEMM_ERR_INVALID_ARG (unknown kind, null pointer), device errors as for the
  * GEMMs, GEMM_ERR_TIMEOUT if the MMAs did not complete within 2 s.
  */
-enum { GEMM_MMA_BF16 = 0, GEMM_MMA_NVFP4 = 1 };
+enum {
+  GEMM_MMA_BF16 = 0,
+  GEMM_MMA_NVFP4 = 1,
+  GEMM_MMA_NVFP4_1CTA_N128 = 2,
+  GEMM_MMA_NVFP4_1CTA_N192 = 3,
+  GEMM_MMA_NVFP4_1CTA_N256 = 4,
+  GEMM_MMA_NVFP4_PAIR_N128 = 5,
+  GEMM_MMA_NVFP4_PAIR_N128_2ACC = 6,
+  GEMM_MMA_MXF4_PAIR_N256 = 7
+};
 int gemm_measure_mma_rate(int kind, double* flop_per_clock_per_sm);
 
 #ifdef __cplusplus

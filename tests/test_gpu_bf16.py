@@ -267,6 +267,22 @@ def test_mma_instruction_rates():
     assert g.get_device_status()[0] == g.GEMM_OK
 
 
+FP4_FORMS = ["GEMM_MMA_NVFP4", "GEMM_MMA_NVFP4_1CTA_N128", "GEMM_MMA_NVFP4_1CTA_N192", "GEMM_MMA_NVFP4_1CTA_N256",
+             "GEMM_MMA_NVFP4_PAIR_N128", "GEMM_MMA_NVFP4_PAIR_N128_2ACC", "GEMM_MMA_MXF4_PAIR_N256"]
+
+
+def test_fp4_instruction_forms(record_property):
+    """Every block-scaled FP4 form a kernel could be built from, measured back to back: each
+    must run (no timeout) at a rate within the nominal FP4 range (4x to 6x of BF16 per
+    clock at most). The figures are printed for the record."""
+    rates = {name: g.measure_mma_rate(getattr(g, name)) for name in FP4_FORMS}
+    for name, r in rates.items():
+        record_property(name, r)
+        print(f"{name}: {r:.0f} FLOP/clk/SM")
+        assert 1000 <= r <= 6.2 * 8192, (name, r)
+    assert g.get_device_status()[0] == g.GEMM_OK
+
+
 @pytest.mark.parametrize("no_pdl", [0, 1])
 def test_dependent_launches_on_one_stream(no_pdl):
     """Back-to-back GEMMs where each reads what the previous one wrote (read after write)
