@@ -127,7 +127,8 @@ def test_group_choice():
 def test_mma_rate_argument_errors():
     import ctypes
     out = ctypes.c_double(0.0)
-    assert g.lib().gemm_measure_mma_rate(7, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.lib().gemm_measure_mma_rate(8, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.lib().gemm_measure_mma_rate(-1, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
     assert g.lib().gemm_measure_mma_rate(g.GEMM_MMA_BF16, None) == g.GEMM_ERR_INVALID_ARG
 
 
