@@ -82,6 +82,8 @@ def recorded_traffic(workload: str, kind: str):
 class ClockSampler:
     """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
 
+    MIN_REGION_S = 0.5
+
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
@@ -161,13 +163,15 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.stop()
         out = self.window(self.t0, self.t1)
-        if out["samples"] == 0:
-            region_ms = (self.t1 - self.t0) * 1e3 if self.t0 and self.t1 else None
-            out["note"] = (f"no nvidia-smi sample fell inside the {region_ms:.1f} ms timed region "
-                           "(100 ms sampling period)" if region_ms is not None else "no sample in the timed region")
+        region_s = (self.t1 - self.t0) if self.t0 and self.t1 else 0.0
+        if region_s < self.MIN_REGION_S:
+            # nvidia-smi reports values averaged over its last period: in a region this short
+            # its few samples (if any) describe the load before the region, not the region
+            out = {"sm_mhz": None, "power_w_median": None, "samples": out["samples"], "reasons": [],
+                   "note": f"the {region_s * 1e3:.1f} ms timed region is shorter than {self.MIN_REGION_S:.1f} s "
+                           "(5 sampling periods of 100 ms): no clock is claimed for it"}
             # the sampler's maximum clock does not depend on load
-            allmax = self.window(float("-inf"), float("inf"))["sm_max_mhz"]
-            out["sm_max_mhz"] = allmax
+            out["sm_max_mhz"] = self.window(float("-inf"), float("inf"))["sm_max_mhz"]
         if after is not None:
             cont = self.window(*after)
             cont["what"] = (f"untimed continuation of the same launches for {(after[1] - after[0]):.2f} s "
@@ -478,7 +482,7 @@ def run_ours(args, cfg, world, rank, local):
     if st != 0:
         raise RuntimeError(f"kernel status {st} ({detail:#x}) in the timed region")
     after = None
-    if clocks and clocks.window(clocks.t0, clocks.t1)["samples"] < 3:
+    if clocks and (clocks.t1 - clocks.t0) < ClockSampler.MIN_REGION_S:
         # A timed region too short for the sampler: the same launches continue, untimed, for
         # about a second, so that the clocks under this load are still on record (labelled
         # apart from the timed region's own samples).

@@ -41,7 +41,7 @@ EXPORTS = (
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
     "gemm_nvfp4_noalloc", "gemm_measure_mma_rate", "gemm_bf16_fused", "gemm_nvfp4_fused", "gemm_nvfp4_blocked_fused",
-    "gemm_bf16_plan", "gemm_clc_rule",
+    "gemm_bf16_plan", "gemm_clc_rule", "gemm_nvfp4_plan",
 )
 
 # gemm_activation_t
@@ -69,6 +69,7 @@ class gemm_options_t(ctypes.Structure):
         ("no_swap_ab", ctypes.c_int),
         ("no_split_k", ctypes.c_int),
         ("clc", ctypes.c_int),
+        ("no_pad_a", ctypes.c_int),
     ]
 
 
@@ -79,9 +80,9 @@ GEMM_CLC_OFF = 2
 
 
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0, clc=GEMM_CLC_AUTO):
+            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0, clc=GEMM_CLC_AUTO, no_pad_a=0):
     return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl,
-                          no_swap_ab, no_split_k, clc)
+                          no_swap_ab, no_split_k, clc, no_pad_a)
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -152,6 +153,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_nvfp4_blocked_fused.restype = I
         l.gemm_bf16_plan.argtypes = [I, I, I, OP, EP, ctypes.POINTER(I), ctypes.POINTER(I)]
         l.gemm_bf16_plan.restype = I
+        l.gemm_nvfp4_plan.argtypes = [I, I, I, OP, ctypes.POINTER(I)]
+        l.gemm_nvfp4_plan.restype = I
         l.gemm_measure_mma_rate.restype = I
         _lib = l
     return _lib
@@ -266,6 +269,14 @@ def bf16_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None, epi: g
     _check(lib().gemm_bf16_plan(M, N, K, _byref_or_null(opts), _byref_or_null(epi), ctypes.byref(swap),
                                 ctypes.byref(tile_n)), "gemm_bf16_plan")
     return swap.value, tile_n.value
+
+
+def nvfp4_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None) -> int:
+    """Rows of A the NVFP4 GEMM kernel reads for this problem: 32 when A is copied into a
+    padded workspace first, else M (host only)."""
+    a_rows = ctypes.c_int()
+    _check(lib().gemm_nvfp4_plan(M, N, K, _byref_or_null(opts), ctypes.byref(a_rows)), "gemm_nvfp4_plan")
+    return a_rows.value
 
 
 def gemm_nvfp4_noalloc(A, SFA, B, SFB, C, M: int, N: int, K: int, stream=None) -> None:

@@ -224,6 +224,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o->no_split_k != 0 && o->no_split_k != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
+  if (o->no_pad_a != 0 && o->no_pad_a != 1) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
@@ -237,6 +238,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->swap_ab = o->no_swap_ab ? 0 : 1;
   r->split_k = o->no_split_k ? 0 : 1;
   r->clc = o->clc;
+  r->pad_a = o->no_pad_a ? 0 : 1;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;
@@ -324,6 +326,16 @@ static int empty_sum_output(void* C, int M, int N, cudaStream_t stream, const Ep
   return GEMM_OK;
 }
 
+// The M rows of packed E2M1 codes (K / 2 bytes each, contiguous) into `dst`, in stream order.
+int copy_rows(void* dst, const void* A, int M, int K, cudaStream_t stream) {
+  if (cudaMemcpyAsync(dst, A, static_cast<size_t>(M) * (static_cast<size_t>(K) / 2), cudaMemcpyDeviceToDevice,
+                      stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_LAUNCH;
+  }
+  return GEMM_OK;
+}
+
 }  // namespace dtcp
 
 using namespace dtcp;
@@ -378,20 +390,29 @@ int gemm_nvfp4_fused(const void* A, const void* SFA, const void* B, const void* 
   if (info == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return empty_sum_output(C, M, N, s, opt.epi, info->num_sms);
-  // Rearrange both scale matrices into the blocked layout in a stream-ordered workspace,
-  // run the blocked GEMM, and free the workspace in stream order behind it.
+  // Rearrange both scale matrices into the blocked layout in a stream-ordered workspace
+  // (and, for few rows, copy A into a padded buffer there), run the blocked GEMM, and free
+  // the workspace in stream order behind it.
   const size_t bytes_a = round_up(static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(M, K)), 256);
-  const size_t bytes_b = static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(N, K));
+  const size_t bytes_b = round_up(static_cast<size_t>(gemm_nvfp4_blocked_scale_bytes(N, K)), 256);
+  const int a_rows = nvfp4_a_rows(M, opt);
+  const size_t bytes_pad = a_rows != M ? static_cast<size_t>(a_rows) * (static_cast<size_t>(K) / 2) : 0;
   cudaMemPool_t pool = workspace_pool(device);
   void* ws = nullptr;
-  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b, pool, s) != cudaSuccess) {
+  if (pool == nullptr || cudaMallocFromPoolAsync(&ws, bytes_a + bytes_b + bytes_pad, pool, s) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_OUT_OF_MEMORY;
   }
   uint8_t* sfa_blk = static_cast<uint8_t*>(ws);
   uint8_t* sfb_blk = sfa_blk + bytes_a;
-  st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s, opt.pdl);
-  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, sfa_blk, B, sfb_blk, C, M, N, K, s, opt);
+  const void* a_src = A;
+  if (bytes_pad > 0) {
+    uint8_t* a_pad = sfb_blk + bytes_b;
+    st = copy_rows(a_pad, A, M, K, s);
+    a_src = a_pad;
+  }
+  if (st == GEMM_OK) st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s, opt.pdl);
+  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(a_src, sfa_blk, B, sfb_blk, C, M, N, K, s, opt, a_rows);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;
 }
@@ -443,7 +464,20 @@ int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void*
   if (info == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (K == 0) return empty_sum_output(C, M, N, s, opt.epi, info->num_sms);
-  return run_gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt);
+  const int a_rows = nvfp4_a_rows(M, opt);
+  if (a_rows == M) return run_gemm_nvfp4_blocked(A, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt);
+  // few rows: A from a padded copy in a stream-ordered workspace, freed in order behind the GEMM
+  cudaMemPool_t pool = workspace_pool(device);
+  void* ws = nullptr;
+  if (pool == nullptr ||
+      cudaMallocFromPoolAsync(&ws, static_cast<size_t>(a_rows) * (static_cast<size_t>(K) / 2), pool, s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_OUT_OF_MEMORY;
+  }
+  st = copy_rows(ws, A, M, K, s);
+  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(ws, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt, a_rows);
+  if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
+  return st;
 }
 
 int gemm_nvfp4_blocked_ex(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
@@ -465,6 +499,14 @@ int gemm_bf16_plan(int M, int N, int K, const gemm_options_t* options, const gem
   if (st != GEMM_OK) return st;
   *swap_ab = bf16_swap_ab(M, N, opt) ? 1 : 0;
   *tile_n = bf16_tile_n(M, N, opt);
+  return GEMM_OK;
+}
+
+int gemm_nvfp4_plan(int M, int N, int K, const gemm_options_t* options, int* a_rows) {
+  RunOptions opt;
+  if (resolve_options(options, &opt) != GEMM_OK || a_rows == nullptr || M < 0 || N < 0 || K < 0)
+    return GEMM_ERR_INVALID_ARG;
+  *a_rows = nvfp4_a_rows(M, opt);
   return GEMM_OK;
 }
 

@@ -22,7 +22,8 @@
 //   warps 4..11 epilogue: warp 4 + 4h + q reads TMEM lanes 32q.. of accumulator columns
 //               128h..128h+127 into registers (four loads, one wait), releases TMEM, then
 //               converts to BF16 and stores 32 x 16 tiles through a 1 KB staging buffer
-//               with TMA (small, so that shared memory holds a sixth stage)
+//               (32-byte swizzled, conflict-free) with TMA (small, so that shared memory
+//               holds a sixth stage)
 //   warps 12..15 scale copiers (leader CTA): copier c copies the scales of MMA c of every
 //               stage (SFA, SFB rows 0-127, SFB rows 128-255) and arrives on sf_ready as
 //               soon as the copies are issued (copies and MMAs run in issue order)
@@ -124,6 +125,7 @@ struct Nvfp4Layout {
   static constexpr int SMEM_BYTES = SMEM_USED + 1024;
 
   static_assert(SMEM_BYTES <= 232448, "exceeds 227 KB of shared memory per CTA");
+  static_assert(OFF_EPI % 1024 == 0 && EPI_BUF_BYTES % 256 == 0, "32-byte swizzled staging needs 256-byte alignment");
   static_assert(SF_TMEM_COL0 + SF_STAGES * SF_COLS <= TMEM_COLS, "scale ring does not fit in TMEM");
   static_assert(A_BYTES + B_BYTES == 32768, "A+B tile bytes per CTA per stage");
   static_assert(STAGE_BYTES == 38912, "38 KB stage of a CTA pair kernel");
@@ -475,7 +477,11 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
           const uint32_t* s = &v[e >> 1][(e & 1) * 16];
           if (lane == 0) bulk_wait_group_read<0>();  // the store that last read `buf` is done
           __syncwarp();
+          // Row `lane` of the 32 x 16 staging tile (32 bytes per row) with the 32-byte swizzle
+          // of the C tensor map: 16-byte chunk j at j ^ (bit 2 of the row). The 8 lanes of a
+          // store phase then cover all 32 banks (without it lanes r and r + 4 collide).
           const uint32_t row_addr = buf + lane * (L::EPI_COLS * 2);
+          const uint32_t c0 = row_addr + (((lane >> 2) & 1u) << 4), c1 = c0 ^ 16u;
           uint32_t pk[8];
           if constexpr (!FUSED) {
 #pragma unroll
@@ -495,8 +501,8 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
                 break;
               }
               cload_phase ^= 1u;
-              ld_shared_v4(row_addr, old[0], old[1], old[2], old[3]);
-              ld_shared_v4(row_addr + 16, old[4], old[5], old[6], old[7]);
+              ld_shared_v4(c0, old[0], old[1], old[2], old[3]);
+              ld_shared_v4(c1, old[4], old[5], old[6], old[7]);
             }
             const uint4 b0 = epi_bias8(p.epi, col, p.N), b1 = epi_bias8(p.epi, col + 8, p.N);
             const uint32_t bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
@@ -504,8 +510,8 @@ __device__ __forceinline__ void epilogue_role(const Nvfp4Params& p, const CUtens
             for (int k = 0; k < 8; ++k) pk[k] = epi_pair(s[2 * k], s[2 * k + 1], old[k], bb[k], p.epi);
             __syncwarp();  // every lane has read its row of the prior C before any lane overwrites it
           }
-          st_shared_v4(row_addr, pk[0], pk[1], pk[2], pk[3]);
-          st_shared_v4(row_addr + 16, pk[4], pk[5], pk[6], pk[7]);
+          st_shared_v4(c0, pk[0], pk[1], pk[2], pk[3]);
+          st_shared_v4(c1, pk[4], pk[5], pk[6], pk[7]);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -685,7 +691,7 @@ int max_active_clusters(int device) {
 }  // namespace
 
 int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const void* SFB, void* C, int M, int N,
-                           int K, cudaStream_t stream, const RunOptions& opt) {
+                           int K, cudaStream_t stream, const RunOptions& opt, int a_rows) {
   int device = 0, err = 0;
   const DeviceInfo* info = current_device_info(&device, &err);
   if (info == nullptr) return err;
@@ -694,8 +700,8 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   CUtensorMap ta, tb, tbh, tsa, tsb, tc;
   const uint64_t kbytes = uint64_t(K) / 2;
   const uint64_t ksteps = uint64_t(K) / 64;
-  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, M, kbytes, NL::BLOCK_K / 2, NL::BLOCK_M,
-                          CU_TENSOR_MAP_SWIZZLE_128B);
+  int st = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, std::max(M, a_rows), kbytes,
+                          NL::BLOCK_K / 2, NL::BLOCK_M, CU_TENSOR_MAP_SWIZZLE_128B);
   if (st == GEMM_OK)
     st = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, N, kbytes, NL::BLOCK_K / 2, NL::B_ROWS,
                         CU_TENSOR_MAP_SWIZZLE_128B);
@@ -715,9 +721,9 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
     const uint32_t box[3] = {128, NL::KSTEPS, 2};
     st = encode_tmap_3d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, SFB, dims, strides, box);
   }
-  if (st == GEMM_OK)  // C stores: 32 rows x 16 columns of BF16 per box
+  if (st == GEMM_OK)  // C stores: 32 rows x 16 columns of BF16 per box, 32-byte swizzle
     st = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, N, M, uint64_t(N) * 2, NL::EPI_COLS, 32,
-                        CU_TENSOR_MAP_SWIZZLE_NONE);
+                        CU_TENSOR_MAP_SWIZZLE_32B);
   if (st != GEMM_OK) return st;
 
   Nvfp4Params p;

@@ -56,6 +56,7 @@ struct RunOptions {
   int swap_ab = 1;  // allow C^T = B A^T for BF16 GEMMs with few rows
   int split_k = 1;  // allow K splits for the swapped BF16 GEMMs
   int clc = 0;      // cluster launch control: 0 = by clc_rule, 1 = on, 2 = off
+  int pad_a = 1;    // NVFP4 with 1 <= M < kNvfp4PadRows: read A from a padded copy
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
   EpilogueOptions epi;
@@ -69,12 +70,23 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
 // Whether run_gemm_bf16 computes C^T = B A^T for this problem, and the tile N it uses.
 bool bf16_swap_ab(int M, int N, const RunOptions& opt);
 int bf16_tile_n(int M, int N, const RunOptions& opt);
+// a_rows: rows of the buffer A points to (>= M): the A tensor map spans them, rows past M
+// reach only C rows that are never stored.
 int run_gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
-                           int M, int N, int K, cudaStream_t stream, const RunOptions& opt);
+                           int M, int N, int K, cudaStream_t stream, const RunOptions& opt, int a_rows = 0);
+
+// NVFP4 GEMMs with fewer rows than this read A from a copy padded to this many rows (see
+// gemm_options_t.no_pad_a): measured on GB300, all-CTA reads of an A that spans less than
+// 32 rows of 4 KB contend for a few L2 slices.
+constexpr int kNvfp4PadRows = 32;
+inline int nvfp4_a_rows(int M, const RunOptions& opt) { return (opt.pad_a && M >= 1 && M < kNvfp4PadRows) ? kNvfp4PadRows : M; }
 int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStream_t stream, int pdl = 1);
 // Both matrices of a GEMM in one launch (rows0 + rows1 row blocks).
 int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
                      cudaStream_t stream, int pdl = 1);
+
+// Device-to-device copy of M rows of packed E2M1 codes (K / 2 bytes each), in stream order.
+int copy_rows(void* dst, const void* A, int M, int K, cudaStream_t stream);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).
 int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,

@@ -70,6 +70,13 @@ extern "C" int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B,
   const size_t bytes_a = round_up_256(static_cast<size_t>(ceil_div(M, 128)) * 128 * (static_cast<size_t>(K) / 16));
   const size_t bytes_b = static_cast<size_t>(ceil_div(N, 128)) * 128 * (static_cast<size_t>(K) / 16);
   if (bytes_a + bytes_b > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_TOO_SMALL;
+  // Few rows: A is read from a copy padded to 32 rows (as gemm_nvfp4 does), placed after the
+  // scales when the array has room for it; otherwise A is read in place.
+  const RunOptions opt;
+  int a_rows = nvfp4_a_rows(M, opt);
+  const size_t off_pad = round_up_256(bytes_a + bytes_b);
+  if (a_rows != M && off_pad + static_cast<size_t>(a_rows) * (static_cast<size_t>(K) / 2) > kNoAllocScratchBytes)
+    a_rows = M;
   int device = 0, err = 0;
   if (current_device_info(&device, &err) == nullptr) return err;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -83,8 +90,15 @@ extern "C" int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B,
   uint8_t* scratch = scratch_address(device);
   if (scratch == nullptr) return GEMM_ERR_NO_DEVICE;
   // The pack kernel writes every byte the GEMM reads (padding rows as zeros), so nothing
-  // left in the array by an earlier call needs clearing.
-  int st = run_pack_scales2(SFA, scratch, M, SFB, scratch + bytes_a, N, K, s);
-  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(A, scratch, B, scratch + bytes_a, C, M, N, K, s, RunOptions());
+  // left in the array by an earlier call needs clearing. (The rows of the padded A past M
+  // keep an earlier call's bytes: they only reach C rows that are never stored.)
+  const void* a_src = A;
+  int st = GEMM_OK;
+  if (a_rows != M) {
+    st = copy_rows(scratch + off_pad, A, M, K, s);
+    a_src = scratch + off_pad;
+  }
+  if (st == GEMM_OK) st = run_pack_scales2(SFA, scratch, M, SFB, scratch + bytes_a, N, K, s);
+  if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(a_src, scratch, B, scratch + bytes_a, C, M, N, K, s, opt, a_rows);
   return st;
 }

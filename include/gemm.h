@@ -228,6 +228,13 @@ typedef struct {
                             is launched, and each running cluster takes the items of clusters it
                             cancels before they start (dynamic tile scheduling); 2 = never: the
                             co-resident clusters walk the items with a fixed stride */
+    int no_pad_a;        /* NVFP4 with 1 <= M < 32 (gemm_nvfp4*, gemm_nvfp4_blocked*): 0 = A's M rows
+                            are first copied (one device-to-device cudaMemcpyAsync) into a
+                            32-row buffer from the library's stream-ordered pool, and the GEMM
+                            reads A from there (rows M..31 are not written; they only reach C
+                            rows that are never stored): spread over 32 rows, A's lines no
+                            longer all fall in the few L2 slices that every CTA pair reads at
+                            once; 1 = never (A read in place, no allocation) */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
@@ -235,8 +242,8 @@ int gemm_bf16_ex(const void* A, const void* B, void* C, int M, int N, int K, voi
                  const gemm_options_t* options);
 
 /* gemm_nvfp4 with explicit options (only persistent, group_m, max_clusters,
- * wait_limit_us, debug_flags, no_tail_split and no_pdl apply; kernel must be
- * GEMM_KERNEL_DEFAULT). */
+ * wait_limit_us, debug_flags, no_tail_split, no_pdl, clc and no_pad_a apply; kernel must
+ * be GEMM_KERNEL_DEFAULT). */
 int gemm_nvfp4_ex(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
                   int M, int N, int K, void* stream, const gemm_options_t* options);
 
@@ -333,6 +340,14 @@ int gemm_choose_group_m(int M, int N, int K, int tile_m, int tile_n, int elem_by
  */
 int gemm_bf16_plan(int M, int N, int K, const gemm_options_t* options, const gemm_epilogue_t* epilogue, int* swap_ab,
                    int* tile_n);
+
+/*
+ * gemm_nvfp4_plan -- host evaluation of the NVFP4 configuration choice (no GPU needed):
+ * *a_rows = the rows of A the GEMM kernel reads: 32 when A is first copied into a padded
+ * 32-row workspace (1 <= M < 32 and options->no_pad_a == 0), else M. options may be NULL.
+ * Returns GEMM_ERR_INVALID_ARG for negative sizes, a null output or invalid options.
+ */
+int gemm_nvfp4_plan(int M, int N, int K, const gemm_options_t* options, int* a_rows);
 
 /* Number of kernel launches this library has issued in this process (all devices). */
 unsigned long long gemm_launch_count(void);

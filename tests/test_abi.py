@@ -172,3 +172,19 @@ def test_clc_rule_bands():
         g.clc_rule(10, 0, 8192)
     with pytest.raises(g.GemmError):
         g.clc_rule(-1, W, 8192)
+
+
+def test_nvfp4_plan_pads_a_for_few_rows():
+    """1 <= M < 32: the NVFP4 GEMM reads A from a 32-row copy, unless no_pad_a; otherwise A in place."""
+    for M in (1, 2, 16, 31):
+        assert g.nvfp4_plan(M, 8192, 8192) == 32
+        assert g.nvfp4_plan(M, 8192, 8192, g.options(no_pad_a=1)) == M
+    for M in (0, 32, 33, 256, 8192):
+        assert g.nvfp4_plan(M, 8192, 8192) == M
+    import ctypes
+    out = ctypes.c_int()
+    assert g.lib().gemm_nvfp4_plan(-1, 8, 256, None, ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, None, None) == g.GEMM_ERR_INVALID_ARG
+    o = g.options()
+    o.no_pad_a = 2
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG

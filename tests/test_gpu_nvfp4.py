@@ -239,6 +239,71 @@ def test_launches_per_call():
     assert g.launch_count() == before + 1
 
 
+# ---------------------------------------------------------------- few rows: A from a padded copy
+
+FEW_ROW_SHAPES = [(1, 264, 512), (7, 1024, 2048), (16, 520, 256), (31, 4104, 1024)]
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("shape", FEW_ROW_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_read_a_from_padded_copy(shape, path):
+    """1 <= M < 32: the GEMM reads A from a 32-row copy (rows M..31 unset). The result must
+    match the oracle, and be bit-identical to reading A in place (no_pad_a = 1): the same
+    rows enter the same MMAs."""
+    M, N, K = shape
+    assert g.nvfp4_plan(M, N, K) == 32 and g.nvfp4_plan(M, N, K, g.options(no_pad_a=1)) == M
+    a, sfa, b, sfb = si.nvfp4_problem(M * 3 + N, M, N, K)
+    padded = run(a, sfa, b, sfb, path)
+    assert_nvfp4_close(padded, oracle.gemm_nvfp4(a, sfa, b, sfb), f"padded {shape} {path}")
+    assert np.array_equal(padded, run(a, sfa, b, sfb, path, no_pad_a=1))
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_few_rows_unit_scales_bit_exact(path):
+    M, N, K = 5, 776, 1024
+    a, _, b, _ = si.nvfp4_problem(12, M, N, K)
+    sfa = torch.full((M, K // 16), E4M3_ONE, dtype=torch.uint8)
+    sfb = torch.full((N, K // 16), E4M3_ONE, dtype=torch.uint8)
+    assert_bf16_exact(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), f"few rows unit scales {path}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_few_rows_guard_band_untouched(path):
+    """The padded rows' products (C rows M..31 of the kernel's view) are never stored."""
+    M, N, K = 3, 264, 512
+    a, sfa, b, sfb = (t.to(DEV) for t in si.nvfp4_problem(24, M, N, K))
+    pad = 40 * N   # more than the 29 rows the padded copy adds
+    buf = torch.full((M * N + 2 * pad,), 12345.0, dtype=torch.bfloat16, device=DEV)
+    sentinel = bits(buf[:pad]).copy()
+    C = buf[pad:pad + M * N].view(M, N)
+    if path == "blocked_scales":
+        g.gemm_nvfp4_blocked(a, g.pack_scales(sfa), b, g.pack_scales(sfb), C, M, N, K)
+    else:
+        g.gemm_nvfp4(a, sfa, b, sfb, C, M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(buf[:pad]), sentinel)
+    assert np.array_equal(bits(buf[pad + M * N:]), sentinel)
+    assert_nvfp4_close(bits(C), oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu()), "few-row guard band")
+
+
+def test_few_rows_fused_epilogue_on_padded_copy():
+    M, N, K = 9, 512, 1024
+    a, sfa, b, sfb = (t.to(DEV) for t in si.nvfp4_problem(25, M, N, K))
+    bias = torch.linspace(-1, 1, N).to(torch.bfloat16).to(DEV)
+    C0 = (torch.arange(M * N, dtype=torch.float32).reshape(M, N) / (M * N) - 0.5).to(torch.bfloat16).to(DEV)
+    out = {}
+    for no_pad in (0, 1):
+        C = C0.clone()
+        g.gemm_nvfp4_fused(a, sfa, b, sfb, C, M, N, K, g.epilogue(0.5, 1.0, bias, g.GEMM_ACT_RELU),
+                           opts=g.options(no_pad_a=no_pad))
+        torch.cuda.synchronize()
+        out[no_pad] = bits(C)
+    assert np.array_equal(out[0], out[1])
+    acc = oracle.gemm_nvfp4(a.cpu(), sfa.cpu(), b.cpu(), sfb.cpu())
+    ref = oracle.epilogue(acc, 0.5, 1.0, bits(C0), bits(bias), oracle.ACT_RELU)
+    assert_nvfp4_close(out[0], ref, "few rows fused")
+
+
 @pytest.mark.parametrize("no_pdl", [0, 1])
 def test_back_to_back_calls_on_one_stream(no_pdl):
     """Consecutive gemm_nvfp4 calls on one stream: each packs its scales into a pooled

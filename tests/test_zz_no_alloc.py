@@ -75,6 +75,21 @@ def test_noalloc_unit_scales_bit_exact_on_two_calls_in_a_row():
     assert g.get_device_status()[0] == g.GEMM_OK
 
 
+def test_noalloc_few_rows_on_two_calls_in_a_row():
+    # fewer than 32 rows: A is copied into the array too (after the scales), padded to 32
+    # rows; the second call, with fewer rows, finds the first call's rows past its own M
+    for seed, (M, N, K) in [(54, (20, 1024, 2048)), (55, (3, 264, 512))]:
+        got, want, ref = _both(seed, M, N, K)
+        assert np.array_equal(got, bits_of(want)), f"noalloc vs gemm_nvfp4 {M}x{N}x{K}"
+        assert_nvfp4_close(got, ref, f"noalloc vs oracle {M}x{N}x{K}")
+    assert g.get_device_status()[0] == g.GEMM_OK
+
+
+def bits_of(values: np.ndarray) -> np.ndarray:
+    """BF16 bit patterns of values that are BF16 numbers (exact conversion)."""
+    return bits(torch.from_numpy(values).to(torch.bfloat16))
+
+
 def test_noalloc_rejects_problems_larger_than_its_scratch():
     K = 16384
     # M = N = 8192 at K = 16384 fills the 16 MiB exactly; one more row block does not fit
