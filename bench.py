@@ -603,8 +603,9 @@ def run_ours(args, cfg, world, rank, local):
         "config": {
             "workload": cfg["workload"], "M": M, "N": N, "K": K,
             "l2_flush": f"rotation over {R} input sets of {sb / 2**20:.0f} MiB (> 2x L2 = {2 * l2 / 2**20:.0f} MiB)",
-            "kernel": {0: "default (2-CTA persistent, 128-K stages)", 1: "1-CTA", 2: "2-CTA, 128-K stages",
-                       3: "2-CTA, 64-K stages"}[args.kernel]
+            "kernel": {0: "default", 1: "1-CTA", 2: "2-CTA, 256 x 256 tile, 128-K stages",
+                       3: "2-CTA, 256 x 256 tile, 64-K stages",
+                       4: "2-CTA, 512 x 256 tile (two 128-row M-waves per CTA), 64-K stages"}[args.kernel]
             + ("" if not args.no_persistent else ", one tile per cluster")
             + (", no tail split" if args.no_tail_split else "")
             + (", plain launches (no programmatic dependent launch)" if args.no_pdl else ""),

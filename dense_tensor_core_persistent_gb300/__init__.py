@@ -34,6 +34,7 @@ GEMM_KERNEL_DEFAULT = 0
 GEMM_KERNEL_BF16_1CTA = 1
 GEMM_KERNEL_BF16_2CTA = 2
 GEMM_KERNEL_BF16_2CTA_K64 = 3
+GEMM_KERNEL_BF16_2CTA_WIDE = 4
 
 # Entry points declared in include/gemm.h (the CPU tests check the library exports all of them).
 EXPORTS = (

@@ -20,7 +20,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libdtcp_gemm.so")
-SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_nvfp4.cu", "pack_scales.cu", "noalloc.cu", "mma_rate.cu"]
+SOURCES = ["api.cu", "gemm_bf16.cu", "gemm_bf16_wide.cu", "gemm_nvfp4.cu", "pack_scales.cu", "noalloc.cu",
+           "mma_rate.cu"]
 HEADERS = ["ptx.cuh", "common.cuh", "schedule.h", "host_common.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v", "-I", os.path.join(ROOT, "include")]

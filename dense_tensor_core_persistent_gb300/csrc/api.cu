@@ -225,7 +225,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pad_a != 0 && o->no_pad_a != 1) return GEMM_ERR_INVALID_ARG;
-  if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_K64) return GEMM_ERR_INVALID_ARG;
+  if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_WIDE) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
   if (o->debug_flags & ~1u) return GEMM_ERR_INVALID_ARG;

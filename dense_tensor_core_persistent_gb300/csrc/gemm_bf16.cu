@@ -892,6 +892,8 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
       return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
     case GEMM_KERNEL_BF16_2CTA_K64:
       return Bf16PairK64::run(A, B, C, M, N, K, stream, opt, device, *info);
+    case GEMM_KERNEL_BF16_2CTA_WIDE:
+      return run_gemm_bf16_wide(A, B, C, M, N, K, stream, opt);
     default:
       return GEMM_ERR_INVALID_ARG;
   }

@@ -67,6 +67,9 @@ cudaMemPool_t workspace_pool(int device);
 
 int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
                   const RunOptions& opt);
+// The 512 x 256 pair tile (two M-waves per CTA); plain epilogue, static schedule.
+int run_gemm_bf16_wide(const void* A, const void* B, void* C, int M, int N, int K, cudaStream_t stream,
+                       const RunOptions& opt);
 // Whether run_gemm_bf16 computes C^T = B A^T for this problem, and the tile N it uses.
 bool bf16_swap_ab(int M, int N, const RunOptions& opt);
 int bf16_tile_n(int M, int N, const RunOptions& opt);

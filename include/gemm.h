@@ -23,11 +23,12 @@
  *   - `stream` is a cudaStream_t / CUstream handle (NULL = legacy default
  *     stream). Calls are asynchronous: they enqueue work and return; nothing
  *     is synchronised. Results are visible to later work on `stream`.
- *   - Device memory: gemm_nvfp4_blocked and gemm_nvfp4_pack_scales allocate
- *     nothing; nor does gemm_bf16, except for a few-row GEMM that splits K (see
- *     gemm_bf16 and gemm_options_t.no_split_k). gemm_nvfp4 takes a temporary workspace for the
- *     rearranged scales from a library-owned, stream-ordered memory pool (see
- *     gemm_nvfp4). The library also holds one process-wide device status word
+ *   - Device memory: gemm_nvfp4_pack_scales allocates nothing; nor do gemm_nvfp4_blocked,
+ *     except for fewer than 32 rows (a padded copy of A; gemm_options_t.no_pad_a), and
+ *     gemm_bf16, except for a few-row GEMM that splits K (see gemm_bf16 and
+ *     gemm_options_t.no_split_k). gemm_nvfp4 takes a temporary workspace for the
+ *     rearranged scales (and the padded A) from a library-owned, stream-ordered memory
+ *     pool (see gemm_nvfp4). The library also holds one process-wide device status word
  *     (a static __device__ variable) that kernels set if a bounded internal
  *     wait expires; read it with gemm_get_device_status.
  *   - Return value: GEMM_OK (0) or a gemm_status_t code for problems found on
@@ -98,7 +99,9 @@ int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* 
  * scale byte must be 0; NaN scales give unspecified results.
  * Launches: one scale-packing kernel (SFA and SFB together) into a workspace of
  * gemm_nvfp4_blocked_scale_bytes(M, K) + gemm_nvfp4_blocked_scale_bytes(N, K)
- * bytes (+ up to 255 bytes of alignment), then the gemm_nvfp4_blocked kernel. The
+ * bytes (+ up to 510 bytes of alignment), then the gemm_nvfp4_blocked kernel; with
+ * 1 <= M < 32 first a device-to-device copy of A into 32 * K / 2 more bytes of the
+ * workspace, which the GEMM reads instead of A (gemm_options_t.no_pad_a). The
  * workspace comes from a library-owned stream-ordered pool (cudaMallocFromPoolAsync)
  * and is returned to it in stream order after the GEMM, so concurrent calls on
  * different streams use different workspaces. Returns GEMM_ERR_OUT_OF_MEMORY if
@@ -132,7 +135,11 @@ int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, vo
  * gemm_nvfp4_blocked -- gemm_nvfp4 with SFA and SFB given in the blocked layout
  * (gemm_nvfp4_blocked_scale_bytes(M, K) and (N, K) bytes). Same operands, result,
  * constraints and errors as gemm_nvfp4. This is the fast path: a stage's scales for
- * 128 rows are one contiguous 2 KB block, loaded by TMA together with the codes.
+ * 128 rows are one contiguous 2 KB block, loaded by TMA together with the codes. With
+ * 1 <= M < 32 the call first copies A into a 32-row buffer of 32 * K / 2 bytes from the
+ * library's stream-ordered pool (returned to it in stream order after the GEMM) and the
+ * GEMM reads A from there (gemm_options_t.no_pad_a = 1 reads A in place and allocates
+ * nothing); GEMM_ERR_OUT_OF_MEMORY if that buffer cannot be obtained.
  */
 int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, const void* SFB_blocked, void* C,
                        int M, int N, int K, void* stream);
@@ -164,8 +171,11 @@ int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, co
  *     contents (each call rewrites all of the part it reads, so nothing needs clearing).
  *     Calls whose work overlaps on the GPU -- on different streams without ordering
  *     between them -- race on it: order them on one stream or with events.
- * Launches: one scale-packing kernel (SFA and SFB together) and the gemm_nvfp4_blocked
- * kernel, on `stream`.
+ *   - with 1 <= M < 32, A's rows are first copied (cudaMemcpyAsync, device to device) into
+ *     the array after the scales, as a 32-row buffer the GEMM reads (gemm_options_t.no_pad_a),
+ *     when the array has room for it (32 * K / 2 more bytes); otherwise A is read in place.
+ * Launches: that copy for few rows, one scale-packing kernel (SFA and SFB together) and
+ * the gemm_nvfp4_blocked kernel, on `stream`.
  */
 #define GEMM_NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
@@ -194,7 +204,12 @@ typedef enum {
     GEMM_KERNEL_BF16_1CTA = 1,      /* BF16, cta_group::1, 128 x 256 tile per CTA */
     GEMM_KERNEL_BF16_2CTA = 2,      /* BF16, cta_group::2, 256 x 256 tile per CTA pair, 3 stages of
                                        128 K (8 MMAs per stage): the default */
-    GEMM_KERNEL_BF16_2CTA_K64 = 3   /* the same with 6 stages of 64 K (4 MMAs per stage) */
+    GEMM_KERNEL_BF16_2CTA_K64 = 3,  /* the same with 6 stages of 64 K (4 MMAs per stage) */
+    GEMM_KERNEL_BF16_2CTA_WIDE = 4  /* BF16, cta_group::2, 512 x 256 tile per CTA pair: each CTA
+                                       holds 256 rows as two 128-row M-waves whose accumulators
+                                       fill TMEM; 4 stages of 64 K; static schedule and plain
+                                       epilogue only (a fused epilogue or clc = 1 is
+                                       GEMM_ERR_INVALID_ARG) */
 } gemm_kernel_t;
 
 typedef struct {

@@ -34,6 +34,8 @@ VARIANTS = {
     "single_cta_persistent": dict(kernel=g.GEMM_KERNEL_BF16_1CTA),
     "pair_k64_persistent": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_K64),
     "pair_k64_tile_per_cluster": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_K64, persistent=0),
+    "pair_wide_persistent": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_WIDE),
+    "pair_wide_tile_per_cluster": dict(kernel=g.GEMM_KERNEL_BF16_2CTA_WIDE, persistent=0),
 }
 
 
@@ -78,7 +80,8 @@ def test_ragged_shapes(variant, shape):
 
 
 @pytest.mark.parametrize("max_clusters,group_m", [(1, 0), (3, 1), (3, 2), (5, 3), (7, 16)])
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64,
+                                    g.GEMM_KERNEL_BF16_2CTA_WIDE])
 def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
     """Few clusters, many tiles each: the stage ring and the two TMEM slots cycle across tiles."""
     M, N, K = 1280, 1024, 456   # 5 x 4 tiles of 256 x 256, 8 K stages (last one partial)
@@ -88,7 +91,8 @@ def test_many_tiles_per_cluster(kernel, max_clusters, group_m):
 
 
 @pytest.mark.parametrize("max_clusters", [16, 9, 19])
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64,
+                                    g.GEMM_KERNEL_BF16_2CTA_WIDE])
 def test_tail_wave_split_into_halves(kernel, max_clusters):
     """A last wave at most half full is computed as N-halves of its tiles (N = 128 MMAs)."""
     M, N, K = 1280, 1000, 328     # 5 x 4 tiles (2-CTA) with a ragged last column block
@@ -224,6 +228,48 @@ def test_c3_shape_integer_inputs_every_element_bit_exact():
     _full_size_every_element(2, 8192, 8192, 8192, kind="int", exact=True)
 
 
+# ---------------------------------------------------------------- the 512 x 256 pair tile (two M-waves per CTA)
+
+WIDE = g.GEMM_KERNEL_BF16_2CTA_WIDE
+
+
+@pytest.mark.parametrize("shape", [(4000, 1000, 520), (1536, 512, 64), (513, 264, 1032), (1, 8, 8)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_wide_tile_integer_inputs_bit_exact(shape):
+    """Integer operands keep every FP32 partial sum exact, so both M-waves of each CTA (rows
+    256r + 128w + lane of a 512-row tile) must reproduce the oracle bit for bit; ragged M
+    cuts the last tile inside a wave, ragged N inside a 32-column store box."""
+    M, N, K = shape
+    A, B = si.bf16_problem(M + 2 * N + K, M, N, K, kind="int")
+    assert_bf16_exact(run(A, B, kernel=WIDE), oracle.gemm_bf16(A, B), f"wide {shape}")
+
+
+@pytest.mark.slow
+def test_wide_tile_c4_every_element():
+    """4000 x 14336 x 4096 from seed 3 on the 512 x 256 tile: all 57.3M outputs. The last
+    row block (rows 3584..4095) holds 416 valid rows: its second CTA's second wave holds
+    rows 3968..3999 and reads zeros past row 3999."""
+    M, N, K = 4000, 14336, 4096
+    A, B = si.bf16_problem(3, M, N, K, device=DEV)
+    C = g.matmul_bf16(A, B, opts=g.options(kernel=WIDE))
+    torch.cuda.synchronize()
+    got = bits(C)
+    Ah, Bh = A.cpu(), B.cpu()
+    for r0 in range(0, M, 1000):
+        assert_bf16_close(got[r0:r0 + 1000], oracle.gemm_bf16(Ah, Bh, r0, r0 + 1000), K, f"wide C4 rows {r0}..")
+
+
+def test_wide_tile_rejects_fused_epilogue_and_clc():
+    A = torch.ones(512, 64, dtype=torch.bfloat16, device=DEV)
+    C = torch.empty(512, 512, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_bf16_fused(A, A, C, 512, 512, 64, g.epilogue(alpha=2.0), opts=g.options(kernel=WIDE))
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_bf16(A, A, C, 512, 512, 64, opts=g.options(kernel=WIDE, clc=g.GEMM_CLC_ON))
+    assert e.value.status == g.GEMM_ERR_INVALID_ARG
+
+
 def test_generator_same_values_on_gpu_and_cpu():
     a_cpu = si.uniform_bf16(3, 0, 257, 129)
     a_gpu = si.uniform_bf16(3, 0, 257, 129, device=DEV)
@@ -240,7 +286,8 @@ def test_one_launch_per_call():
     assert g.launch_count() == before + 1
 
 
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_BF16_2CTA, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_K64,
+                                    g.GEMM_KERNEL_BF16_2CTA_WIDE])
 def test_bounded_wait_reports_timeout_and_context_survives(kernel):
     """debug flag 1: the MMA issuer waits on a barrier nothing arrives on. The bounded wait
     expires (100 ms), the kernel records GEMM_ERR_TIMEOUT and exits; the context stays usable."""
