@@ -326,16 +326,6 @@ static int empty_sum_output(void* C, int M, int N, cudaStream_t stream, const Ep
   return GEMM_OK;
 }
 
-// The M rows of packed E2M1 codes (K / 2 bytes each, contiguous) into `dst`, in stream order.
-int copy_rows(void* dst, const void* A, int M, int K, cudaStream_t stream) {
-  if (cudaMemcpyAsync(dst, A, static_cast<size_t>(M) * (static_cast<size_t>(K) / 2), cudaMemcpyDeviceToDevice,
-                      stream) != cudaSuccess) {
-    cudaGetLastError();
-    return GEMM_ERR_LAUNCH;
-  }
-  return GEMM_OK;
-}
-
 }  // namespace dtcp
 
 using namespace dtcp;
@@ -405,13 +395,11 @@ int gemm_nvfp4_fused(const void* A, const void* SFA, const void* B, const void* 
   }
   uint8_t* sfa_blk = static_cast<uint8_t*>(ws);
   uint8_t* sfb_blk = sfa_blk + bytes_a;
-  const void* a_src = A;
-  if (bytes_pad > 0) {
-    uint8_t* a_pad = sfb_blk + bytes_b;
-    st = copy_rows(a_pad, A, M, K, s);
-    a_src = a_pad;
-  }
-  if (st == GEMM_OK) st = run_pack_scales2(SFA, sfa_blk, M, SFB, sfb_blk, N, K, s, opt.pdl);
+  // (few rows: the packing launch also copies A's rows into the padded buffer)
+  uint8_t* a_pad = bytes_pad > 0 ? sfb_blk + bytes_b : nullptr;
+  st = run_pack_scales2_copy(SFA, sfa_blk, M, SFB, sfb_blk, N, K, A, a_pad,
+                             a_pad ? static_cast<long long>(M) * (K / 2) : 0, s, opt.pdl);
+  const void* a_src = a_pad ? a_pad : A;
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(a_src, sfa_blk, B, sfb_blk, C, M, N, K, s, opt, a_rows);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;
@@ -474,7 +462,7 @@ int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void*
     cudaGetLastError();
     return GEMM_ERR_OUT_OF_MEMORY;
   }
-  st = copy_rows(ws, A, M, K, s);
+  st = run_copy_rows(ws, A, M, K, s, opt.pdl);
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(ws, SFA_blocked, B, SFB_blocked, C, M, N, K, s, opt, a_rows);
   if (cudaFreeAsync(ws, s) != cudaSuccess && st == GEMM_OK) st = GEMM_ERR_LAUNCH;
   return st;

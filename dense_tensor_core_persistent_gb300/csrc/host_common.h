@@ -88,8 +88,13 @@ int run_pack_scales(const void* SF, void* SF_blocked, int rows, int K, cudaStrea
 int run_pack_scales2(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
                      cudaStream_t stream, int pdl = 1);
 
-// Device-to-device copy of M rows of packed E2M1 codes (K / 2 bytes each), in stream order.
-int copy_rows(void* dst, const void* A, int M, int K, cudaStream_t stream);
+// The same, plus a copy of copy_bytes (a multiple of 16) from copy_src to copy_dst by extra
+// CTAs of the launch (the few rows of A that the GEMM reads from a padded buffer).
+int run_pack_scales2_copy(const void* SF0, void* out0, int rows0, const void* SF1, void* out1, int rows1, int K,
+                          const void* copy_src, void* copy_dst, long long copy_bytes, cudaStream_t stream, int pdl = 1);
+// Copy of M rows of packed E2M1 codes (K / 2 bytes each, K % 256 == 0) by a kernel launched
+// with programmatic stream serialization (the GEMM after it starts its set-up early).
+int run_copy_rows(void* dst, const void* A, int M, int K, cudaStream_t stream, int pdl = 1);
 
 // Group size along M for the persistent tile order (see gemm_choose_group_m).
 int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per_row_elem,

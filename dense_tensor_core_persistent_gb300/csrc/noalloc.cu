@@ -92,13 +92,10 @@ extern "C" int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B,
   // The pack kernel writes every byte the GEMM reads (padding rows as zeros), so nothing
   // left in the array by an earlier call needs clearing. (The rows of the padded A past M
   // keep an earlier call's bytes: they only reach C rows that are never stored.)
-  const void* a_src = A;
-  int st = GEMM_OK;
-  if (a_rows != M) {
-    st = copy_rows(scratch + off_pad, A, M, K, s);
-    a_src = scratch + off_pad;
-  }
-  if (st == GEMM_OK) st = run_pack_scales2(SFA, scratch, M, SFB, scratch + bytes_a, N, K, s);
+  uint8_t* a_pad = a_rows != M ? scratch + off_pad : nullptr;
+  int st = run_pack_scales2_copy(SFA, scratch, M, SFB, scratch + bytes_a, N, K, A, a_pad,
+                                 a_pad ? static_cast<long long>(M) * (K / 2) : 0, s);
+  const void* a_src = a_pad ? a_pad : A;
   if (st == GEMM_OK) st = run_gemm_nvfp4_blocked(a_src, scratch, B, scratch + bytes_a, C, M, N, K, s, opt, a_rows);
   return st;
 }

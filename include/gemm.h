@@ -100,7 +100,7 @@ int gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, void* 
  * Launches: one scale-packing kernel (SFA and SFB together) into a workspace of
  * gemm_nvfp4_blocked_scale_bytes(M, K) + gemm_nvfp4_blocked_scale_bytes(N, K)
  * bytes (+ up to 510 bytes of alignment), then the gemm_nvfp4_blocked kernel; with
- * 1 <= M < 32 first a device-to-device copy of A into 32 * K / 2 more bytes of the
+ * 1 <= M < 32 the packing launch also copies A into 32 * K / 2 more bytes of the
  * workspace, which the GEMM reads instead of A (gemm_options_t.no_pad_a). The
  * workspace comes from a library-owned stream-ordered pool (cudaMallocFromPoolAsync)
  * and is returned to it in stream order after the GEMM, so concurrent calls on
@@ -136,7 +136,8 @@ int gemm_nvfp4_pack_scales(const void* SF, void* SF_blocked, int rows, int K, vo
  * (gemm_nvfp4_blocked_scale_bytes(M, K) and (N, K) bytes). Same operands, result,
  * constraints and errors as gemm_nvfp4. This is the fast path: a stage's scales for
  * 128 rows are one contiguous 2 KB block, loaded by TMA together with the codes. With
- * 1 <= M < 32 the call first copies A into a 32-row buffer of 32 * K / 2 bytes from the
+ * 1 <= M < 32 the call first copies A (one small copy kernel launched ahead of the GEMM)
+ * into a 32-row buffer of 32 * K / 2 bytes from the
  * library's stream-ordered pool (returned to it in stream order after the GEMM) and the
  * GEMM reads A from there (gemm_options_t.no_pad_a = 1 reads A in place and allocates
  * nothing); GEMM_ERR_OUT_OF_MEMORY if that buffer cannot be obtained.
@@ -171,11 +172,11 @@ int gemm_nvfp4_blocked(const void* A, const void* SFA_blocked, const void* B, co
  *     contents (each call rewrites all of the part it reads, so nothing needs clearing).
  *     Calls whose work overlaps on the GPU -- on different streams without ordering
  *     between them -- race on it: order them on one stream or with events.
- *   - with 1 <= M < 32, A's rows are first copied (cudaMemcpyAsync, device to device) into
- *     the array after the scales, as a 32-row buffer the GEMM reads (gemm_options_t.no_pad_a),
- *     when the array has room for it (32 * K / 2 more bytes); otherwise A is read in place.
- * Launches: that copy for few rows, one scale-packing kernel (SFA and SFB together) and
- * the gemm_nvfp4_blocked kernel, on `stream`.
+ *   - with 1 <= M < 32, A's rows are also copied (by the packing launch) into the array after
+ *     the scales, as a 32-row buffer the GEMM reads (gemm_options_t.no_pad_a), when the
+ *     array has room for it (32 * K / 2 more bytes); otherwise A is read in place.
+ * Launches: one scale-packing kernel (SFA and SFB together; for few rows also the copy of
+ * A) and the gemm_nvfp4_blocked kernel, on `stream`.
  */
 #define GEMM_NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int gemm_nvfp4_noalloc(const void* A, const void* SFA, const void* B, const void* SFB, void* C,
@@ -244,8 +245,10 @@ typedef struct {
                             cancels before they start (dynamic tile scheduling); 2 = never: the
                             co-resident clusters walk the items with a fixed stride */
     int no_pad_a;        /* NVFP4 with 1 <= M < 32 (gemm_nvfp4*, gemm_nvfp4_blocked*): 0 = A's M rows
-                            are first copied (one device-to-device cudaMemcpyAsync) into a
-                            32-row buffer from the library's stream-ordered pool, and the GEMM
+                            are first copied (by the scale-packing launch, or by a small copy
+                            kernel) into a 32-row buffer from the library's stream-ordered pool
+                            (measured on GB300: 46.1 -> 34.9 us at M = 1, N = 28672, K = 8192,
+                            blocked scales), and the GEMM
                             reads A from there (rows M..31 are not written; they only reach C
                             rows that are never stored): spread over 32 rows, A's lines no
                             longer all fall in the few L2 slices that every CTA pair reads at

@@ -258,6 +258,25 @@ def test_few_rows_read_a_from_padded_copy(shape, path):
     assert np.array_equal(padded, run(a, sfa, b, sfb, path, no_pad_a=1))
 
 
+def test_few_rows_launches_per_call():
+    """Fewer than 32 rows: gemm_nvfp4's packing launch also copies A (2 launches in all);
+    gemm_nvfp4_blocked launches a copy kernel before the GEMM (2); with no_pad_a, 2 and 1."""
+    M, N, K = 12, 264, 512
+    a, sfa, b, sfb = si.nvfp4_problem(7, M, N, K, device=DEV)
+    pa, pb = g.pack_scales(sfa), g.pack_scales(sfb)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    torch.cuda.synchronize()
+    for no_pad, want_row, want_blk in ((0, 2, 2), (1, 2, 1)):
+        opts = g.options(no_pad_a=no_pad)
+        before = g.launch_count()
+        g.gemm_nvfp4(a, sfa, b, sfb, C, M, N, K, opts=opts)
+        assert g.launch_count() == before + want_row
+        before = g.launch_count()
+        g.gemm_nvfp4_blocked(a, pa, b, pb, C, M, N, K, opts=opts)
+        assert g.launch_count() == before + want_blk
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_few_rows_unit_scales_bit_exact(path):
     M, N, K = 5, 776, 1024
