@@ -399,6 +399,19 @@ def metric_name(cfg):
     return f"NVFP4 GEMM TFLOP/s @ M={cfg['M']} N={cfg['N']} K={cfg['K']} on 1 GB300"
 
 
+def default_kernel(g, cfg, props, args):
+    """What the library's default kernel choice is for this workload."""
+    M, N, K = cfg["M"], cfg["N"], cfg["K"]
+    if cfg["kind"] == "nvfp4":
+        return "2-CTA, 256 x 256 tile, 6 stages of 256 K"
+    if g.bf16_plan(M, N, K)[0]:
+        return "C^T = B A^T (few rows)"
+    wide = (args.epilogue == "none" and args.clc != "on" and not args.no_persistent and not args.max_clusters
+            and g.bf16_wide_rule(M, N, K, props.multi_processor_count // 2))
+    return ("2-CTA, 512 x 256 tile (two 128-row M-waves per CTA), 64-K stages" if wide
+            else "2-CTA, 256 x 256 tile, 128-K stages")
+
+
 def run_ours(args, cfg, world, rank, local):
     import torch
 
@@ -603,7 +616,8 @@ def run_ours(args, cfg, world, rank, local):
         "config": {
             "workload": cfg["workload"], "M": M, "N": N, "K": K,
             "l2_flush": f"rotation over {R} input sets of {sb / 2**20:.0f} MiB (> 2x L2 = {2 * l2 / 2**20:.0f} MiB)",
-            "kernel": {0: "default", 1: "1-CTA", 2: "2-CTA, 256 x 256 tile, 128-K stages",
+            "kernel": {0: "default: " + default_kernel(g, cfg, props, args), 1: "1-CTA",
+                       2: "2-CTA, 256 x 256 tile, 128-K stages",
                        3: "2-CTA, 256 x 256 tile, 64-K stages",
                        4: "2-CTA, 512 x 256 tile (two 128-row M-waves per CTA), 64-K stages"}[args.kernel]
             + ("" if not args.no_persistent else ", one tile per cluster")

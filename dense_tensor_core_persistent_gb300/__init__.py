@@ -42,7 +42,7 @@ EXPORTS = (
     "gemm_nvfp4_ex", "gemm_tile_coord", "gemm_choose_group_m", "gemm_launch_count",
     "gemm_nvfp4_blocked_scale_bytes", "gemm_nvfp4_pack_scales", "gemm_nvfp4_blocked", "gemm_nvfp4_blocked_ex",
     "gemm_nvfp4_noalloc", "gemm_measure_mma_rate", "gemm_bf16_fused", "gemm_nvfp4_fused", "gemm_nvfp4_blocked_fused",
-    "gemm_bf16_plan", "gemm_clc_rule", "gemm_nvfp4_plan",
+    "gemm_bf16_plan", "gemm_clc_rule", "gemm_nvfp4_plan", "gemm_bf16_wide_rule",
 )
 
 # gemm_activation_t
@@ -156,6 +156,8 @@ def lib() -> ctypes.CDLL:
         l.gemm_bf16_plan.restype = I
         l.gemm_nvfp4_plan.argtypes = [I, I, I, OP, ctypes.POINTER(I)]
         l.gemm_nvfp4_plan.restype = I
+        l.gemm_bf16_wide_rule.argtypes = [I, I, I, I]
+        l.gemm_bf16_wide_rule.restype = I
         l.gemm_measure_mma_rate.restype = I
         _lib = l
     return _lib
@@ -270,6 +272,15 @@ def bf16_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None, epi: g
     _check(lib().gemm_bf16_plan(M, N, K, _byref_or_null(opts), _byref_or_null(epi), ctypes.byref(swap),
                                 ctypes.byref(tile_n)), "gemm_bf16_plan")
     return swap.value, tile_n.value
+
+
+def bf16_wide_rule(M: int, N: int, K: int, wave: int = 76) -> bool:
+    """Whether gemm_bf16's default kernel takes the 512 x 256 pair tile for this problem
+    (plain epilogue, static schedule, not swapped), with `wave` co-resident clusters."""
+    r = lib().gemm_bf16_wide_rule(M, N, K, wave)
+    if r < 0:
+        raise GemmError(-r, "gemm_bf16_wide_rule")
+    return r == 1
 
 
 def nvfp4_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None) -> int:

@@ -563,6 +563,11 @@ int gemm_clc_rule(int items, int wave, int K, int nvfp4) {
   return clc_rule(items, wave, K, nvfp4 != 0) ? 1 : 0;
 }
 
+int gemm_bf16_wide_rule(int M, int N, int K, int wave) {
+  if (M < 0 || N < 0 || K < 0 || wave <= 0) return -GEMM_ERR_INVALID_ARG;
+  return wide_rule(M, N, K, wave) ? 1 : 0;
+}
+
 unsigned long long gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 }  // extern "C"

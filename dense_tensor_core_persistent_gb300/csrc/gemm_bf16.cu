@@ -869,6 +869,16 @@ bool bf16_swap_ab(int M, int N, const RunOptions& opt) {
   return opt.swap_ab && opt.kernel == GEMM_KERNEL_DEFAULT && M >= 1 && M <= 128 && N >= 256;
 }
 
+// The default kernel for a GEMM that is not swapped: the 512 x 256 pair tile where
+// wide_rule favours it, for the plain epilogue and a static schedule (the 256 x 256 kernel
+// holds the fused epilogue and cluster launch control).
+bool bf16_use_wide(int M, int N, int K, const RunOptions& opt, int wave) {
+  if (opt.kernel != GEMM_KERNEL_DEFAULT || opt.epi.fused() || !opt.persistent || opt.max_clusters > 0) return false;
+  if (bf16_swap_ab(M, N, opt)) return false;
+  if (opt.clc == 1) return false;
+  return wide_rule(M, N, K, wave);
+}
+
 int bf16_tile_n(int M, int N, const RunOptions& opt) {
   if (!bf16_swap_ab(M, N, opt)) return opt.kernel == GEMM_KERNEL_BF16_1CTA ? Bf16OneCta::L::BLOCK_N : Bf16Pair::L::BLOCK_N;
   return M <= 64 ? Bf16Swap64::L::BLOCK_N : Bf16Swap128::L::BLOCK_N;
@@ -887,6 +897,8 @@ int run_gemm_bf16(const void* A, const void* B, void* C, int M, int N, int K, cu
         if (M <= 64) return Bf16Swap64::run(B, A, C, N, M, K, stream, opt, device, *info);
         return Bf16Swap128::run(B, A, C, N, M, K, stream, opt, device, *info);
       }
+      if (bf16_use_wide(M, N, K, opt, Bf16Pair::max_active_clusters(device)))
+        return run_gemm_bf16_wide(A, B, C, M, N, K, stream, opt);
       return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);
     case GEMM_KERNEL_BF16_2CTA:
       return Bf16Pair::run(A, B, C, M, N, K, stream, opt, device, *info);

@@ -72,6 +72,9 @@ int run_gemm_bf16_wide(const void* A, const void* B, void* C, int M, int N, int 
                        const RunOptions& opt);
 // Whether run_gemm_bf16 computes C^T = B A^T for this problem, and the tile N it uses.
 bool bf16_swap_ab(int M, int N, const RunOptions& opt);
+// Whether the default kernel runs this (unswapped) GEMM on the 512 x 256 pair tile, with
+// `wave` co-resident clusters.
+bool bf16_use_wide(int M, int N, int K, const RunOptions& opt, int wave);
 int bf16_tile_n(int M, int N, const RunOptions& opt);
 // a_rows: rows of the buffer A points to (>= M): the A tensor map spans them, rows past M
 // reach only C rows that are never stored.

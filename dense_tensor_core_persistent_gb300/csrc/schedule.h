@@ -83,6 +83,35 @@ DTCP_HD int tail_split_tiles(int num_tiles, int clusters) {
 // K >= 16384, for another kernel on another GPU.)
 DTCP_HD bool clc_rule(int items, int wave, int K, bool nvfp4) { return !nvfp4 && items > wave && K >= 16384; }
 
+// Tile-times a static persistent launch of `tiles` equal tiles takes on `wave` co-resident
+// clusters: its full waves, plus a last partial wave that runs either as whole tiles (one
+// tile-time) or, when its tiles' N-halves fit in one wave (tail_split_tiles), as halves,
+// which take about 0.8 of a tile's time (measured on GB300 for BF16: an N = 128 MMA costs
+// the issuing thread nearly as much as an N = 256 one).
+inline double launch_tile_times(long long tiles, long long wave) {
+  if (tiles <= 0 || wave <= 0) return 0.0;
+  const long long full = tiles / wave, tail = tiles % wave;
+  if (tail == 0) return static_cast<double>(full);
+  return static_cast<double>(full) + ((wave > 1 && 2 * tail <= wave) ? 0.8 : 1.0);
+}
+
+// Whether a plain BF16 GEMM runs on the 512 x 256 pair tile (two 128-row M-waves per CTA)
+// rather than the 256 x 256 one, with `wave` co-resident clusters of either. The wide tile
+// moves a quarter fewer bytes from L2 per FLOP and keeps one more stage in flight, and ran
+// 2-5% faster per tile on GB300 (8192^3, 6144^3, 4000 x 14336 x 4096), but has half as
+// many tiles to spread over the clusters and one accumulator (its tile boundary waits for
+// the epilogue to read TMEM, about 1% of a tile at K = 8192). So: K >= 2048, and the
+// estimated time in tile-times, each wide tile counting 2 / 1.04 standard ones, is lower.
+// (4096^3: 256 tiles of 256 x 256 take 3.8 tile-times on 76 clusters, 128 wide ones 2
+// waves = 3.85: standard; measured 1.5% in its favour.)
+inline bool wide_rule(int M, int N, int K, int wave) {
+  if (K < 2048 || wave < 1 || M < 1 || N < 1) return false;
+  const long long nb = (N + 255) / 256;
+  const long long tiles_std = static_cast<long long>((M + 255) / 256) * nb;
+  const long long tiles_wide = static_cast<long long>((M + 511) / 512) * nb;
+  return 2.0 * launch_tile_times(tiles_wide, wave) / 1.04 < launch_tile_times(tiles_std, wave);
+}
+
 // mode: 0 = clc_rule, 1 = always, 2 = never.
 DTCP_HD bool use_clc(int mode, int items, int wave, int K, bool nvfp4) {
   return mode == 1 ? true : (mode == 2 ? false : clc_rule(items, wave, K, nvfp4));

@@ -325,6 +325,20 @@ int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void*
 int gemm_clc_rule(int items, int wave, int K, int nvfp4);
 
 /*
+ * gemm_bf16_wide_rule -- whether gemm_bf16 (default kernel, plain epilogue, static schedule,
+ * not swapped) computes this problem on the 512 x 256 pair tile (GEMM_KERNEL_BF16_2CTA_WIDE)
+ * rather than the 256 x 256 one, with `wave` co-resident clusters (76 on a 152-SM GB300).
+ * Host evaluation, no GPU needed. The rule ("Achieve cuBLAS Performance on NVIDIA GB300 for
+ * HGEMM", v7: the larger tile moves fewer bytes per FLOP; the choice by wave quantization is
+ * this library's): K >= 2048, and the launch's estimated length in 256 x 256 tile-times is
+ * shorter with wide tiles, each counting 2 / 1.04 of a 256 x 256 one (measured 2-5% faster
+ * per tile); a launch of T tiles on W clusters lasts floor(T / W) tile-times plus, for a
+ * partial last wave, 1 (or 0.8 when its tiles run as N-halves, 2 (T mod W) <= W).
+ * Returns 1 or 0; -GEMM_ERR_INVALID_ARG if a size is negative or wave <= 0.
+ */
+int gemm_bf16_wide_rule(int M, int N, int K, int wave);
+
+/*
  * gemm_tile_coord -- host evaluation of the persistent tile order used by the
  * kernels (no GPU needed). The output is split into ceil(M/tile_m) x
  * ceil(N/tile_n) tiles; tile index t (0 <= t < tiles) is mapped to the block

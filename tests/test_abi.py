@@ -188,3 +188,17 @@ def test_nvfp4_plan_pads_a_for_few_rows():
     o = g.options()
     o.no_pad_a = 2
     assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+
+
+def test_bf16_wide_rule():
+    """The 512 x 256 pair tile where its fewer, larger tiles still fill the 76 clusters."""
+    assert g.bf16_wide_rule(8192, 8192, 8192)          # 512 wide tiles: 7 waves vs 13.8
+    assert g.bf16_wide_rule(4000, 14336, 4096)         # 448: 6 waves vs 12
+    assert g.bf16_wide_rule(6144, 6144, 6144)          # 288: 4 waves vs 8
+    assert not g.bf16_wide_rule(4096, 4096, 4096)      # 128: 2 waves vs 3.8 tile-times
+    assert not g.bf16_wide_rule(8192, 8192, 1024)      # shallow K: the tile boundary costs too much
+    assert not g.bf16_wide_rule(512, 512, 8192)        # 2 wide tiles vs 4 tiles, both as N-halves
+    with pytest.raises(g.GemmError):
+        g.bf16_wide_rule(8, 8, 8, 0)
+    l = g.lib()
+    assert l.gemm_bf16_wide_rule(-1, 8, 8, 76) == -g.GEMM_ERR_INVALID_ARG
