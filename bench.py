@@ -40,7 +40,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 CLC_MODES = {"auto": 0, "on": 1, "off": 2}   # gemm_options_t.clc
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor rates (6x)
 KERNEL_SOURCES = {
-    "bf16": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu"],
+    "bf16": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_bf16.cu", "csrc/gemm_bf16_wide.cu"],
     "nvfp4": ["csrc/ptx.cuh", "csrc/common.cuh", "csrc/schedule.h", "csrc/gemm_nvfp4.cu"],
 }
 

@@ -208,8 +208,11 @@ int choose_group_m(int M, int N, int K, int tile_m, int tile_n, double bytes_per
   int g = static_cast<int>(std::lround(std::sqrt(double(c) * w_b / w_a)));
   g = std::min(std::max(g, 1), num_m);
   auto footprint = [&](int gg) { return gg * w_a + std::ceil(double(c) / gg) * w_b; };
-  // Shrink toward balance-preserving smaller groups while the wave does not fit in L2.
-  while (g > 1 && footprint(g) > double(l2_bytes)) --g;
+  // Shrink while the two waves' operands do not fit in L2 and a smaller group still has a
+  // smaller footprint (the rounding of the square root may leave it one step off the
+  // smallest). Once nothing fits, the balanced group still re-reads least: each wave reads
+  // g A tiles and c/g B tiles per K block from DRAM, with no reuse across waves either way.
+  while (g > 1 && footprint(g) > double(l2_bytes) && footprint(g - 1) < footprint(g)) --g;
   return g;
 }
 

@@ -97,19 +97,21 @@ inline double launch_tile_times(long long tiles, long long wave) {
 
 // Whether a plain BF16 GEMM runs on the 512 x 256 pair tile (two 128-row M-waves per CTA)
 // rather than the 256 x 256 one, with `wave` co-resident clusters of either. The wide tile
-// moves a quarter fewer bytes from L2 per FLOP and keeps one more stage in flight, and ran
-// 2-5% faster per tile on GB300 (8192^3, 6144^3, 4000 x 14336 x 4096), but has half as
-// many tiles to spread over the clusters and one accumulator (its tile boundary waits for
-// the epilogue to read TMEM, about 1% of a tile at K = 8192). So: K >= 2048, and the
-// estimated time in tile-times, each wide tile counting 2 / 1.04 standard ones, is lower.
-// (4096^3: 256 tiles of 256 x 256 take 3.8 tile-times on 76 clusters, 128 wide ones 2
-// waves = 3.85: standard; measured 1.5% in its favour.)
+// moves a quarter fewer bytes from L2 per FLOP and keeps one more stage in flight, but has
+// half as many tiles to spread over the clusters and one accumulator (its tile boundary
+// waits for the epilogue to read TMEM). So: K >= 2048, and the estimated time in
+// tile-times is lower, a wide tile counting 2 / f of a 256 x 256 one. f is what a wide
+// tile gained per unit of work in sustained runs on GB300 (under the 1.4 kW power cap,
+// where its smaller data movement also buys clock): 1.035 at K = 2048 (8192^2 x 2048),
+// 1.05-1.08 from K = 4096 (4096^3, 2048 x 8192^2, 3072^2 x 8192, 16384 x 8192^2), so
+// f = 1.03 below K = 4096 and 1.06 from there.
 inline bool wide_rule(int M, int N, int K, int wave) {
   if (K < 2048 || wave < 1 || M < 1 || N < 1) return false;
+  const double f = K < 4096 ? 1.03 : 1.06;
   const long long nb = (N + 255) / 256;
   const long long tiles_std = static_cast<long long>((M + 255) / 256) * nb;
   const long long tiles_wide = static_cast<long long>((M + 511) / 512) * nb;
-  return 2.0 * launch_tile_times(tiles_wide, wave) / 1.04 < launch_tile_times(tiles_std, wave);
+  return 2.0 * launch_tile_times(tiles_wide, wave) / f < launch_tile_times(tiles_std, wave);
 }
 
 // mode: 0 = clc_rule, 1 = always, 2 = never.

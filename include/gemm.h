@@ -331,9 +331,10 @@ int gemm_clc_rule(int items, int wave, int K, int nvfp4);
  * Host evaluation, no GPU needed. The rule ("Achieve cuBLAS Performance on NVIDIA GB300 for
  * HGEMM", v7: the larger tile moves fewer bytes per FLOP; the choice by wave quantization is
  * this library's): K >= 2048, and the launch's estimated length in 256 x 256 tile-times is
- * shorter with wide tiles, each counting 2 / 1.04 of a 256 x 256 one (measured 2-5% faster
- * per tile); a launch of T tiles on W clusters lasts floor(T / W) tile-times plus, for a
- * partial last wave, 1 (or 0.8 when its tiles run as N-halves, 2 (T mod W) <= W).
+ * shorter with wide tiles, each counting 2 / f of a 256 x 256 one, f = 1.03 for K < 4096 and
+ * 1.06 from K = 4096 (the per-work gain measured in sustained runs); a launch of T tiles on
+ * W clusters lasts floor(T / W) tile-times plus, for a partial last wave, 1 (or 0.8 when its
+ * tiles run as N-halves, 2 (T mod W) <= W).
  * Returns 1 or 0; -GEMM_ERR_INVALID_ARG if a size is negative or wave <= 0.
  */
 int gemm_bf16_wide_rule(int M, int N, int K, int wave);

@@ -118,9 +118,11 @@ def test_group_choice():
     # of M; larger ones balance two waves like BF16
     assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 76, L2) == 32
     assert g.choose_group_m(16384, 16384, 16384, 256, 256, 1, 76, L2) == 12
-    # a very large K shrinks the group until two waves' operands fit
-    gl = g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 76, L2)
-    assert 1 <= gl < 12
+    # beyond L2 (a very large K, or the 512 x 256 tile at 8192^3) the balanced group stays:
+    # smaller groups only re-read B more often
+    assert g.choose_group_m(8192, 8192, 65536, 256, 256, 4, 76, L2) == 12
+    assert g.choose_group_m(12288, 12288, 12288, 256, 256, 4, 76, L2) == 12
+    assert g.choose_group_m(8192, 8192, 8192, 512, 256, 4, 76, L2) == 9
     assert g.choose_group_m(8192, 8192, 8192, 256, 256, 1, 74, L2) >= 1
 
 
@@ -195,9 +197,11 @@ def test_bf16_wide_rule():
     assert g.bf16_wide_rule(8192, 8192, 8192)          # 512 wide tiles: 7 waves vs 13.8
     assert g.bf16_wide_rule(4000, 14336, 4096)         # 448: 6 waves vs 12
     assert g.bf16_wide_rule(6144, 6144, 6144)          # 288: 4 waves vs 8
-    assert not g.bf16_wide_rule(4096, 4096, 4096)      # 128: 2 waves vs 3.8 tile-times
+    assert g.bf16_wide_rule(4096, 4096, 4096)          # 128: 2 waves = 3.77 vs 3.8 tile-times
+    assert g.bf16_wide_rule(8192, 8192, 2048)          # 7 waves = 13.6 vs 13.8 (f = 1.03 at K = 2048)
     assert not g.bf16_wide_rule(8192, 8192, 1024)      # shallow K: the tile boundary costs too much
     assert not g.bf16_wide_rule(512, 512, 8192)        # 2 wide tiles vs 4 tiles, both as N-halves
+    assert not g.bf16_wide_rule(2048, 2048, 8192)      # 32 wide tiles as N-halves: 1.51 vs 64 tiles: 1
     with pytest.raises(g.GemmError):
         g.bf16_wide_rule(8, 8, 8, 0)
     l = g.lib()
