@@ -259,6 +259,15 @@ def test_wide_tile_c4_every_element():
         assert_bf16_close(got[r0:r0 + 1000], oracle.gemm_bf16(Ah, Bh, r0, r0 + 1000), K, f"wide C4 rows {r0}..")
 
 
+def test_default_takes_wide_tile_on_ragged_shape():
+    """The default kernel choice at a ragged shape the wide-tile rule selects (72 tiles of
+    512 x 256 in one wave, the last row and column blocks cut), against the oracle."""
+    M, N, K = 2600, 3064, 4104
+    assert g.bf16_wide_rule(M, N, K)
+    A, B = si.bf16_problem(17, M, N, K)
+    assert_bf16_close(run(A, B), oracle.gemm_bf16(A, B), K, "default, wide tile")
+
+
 def test_wide_tile_rejects_fused_epilogue_and_clc():
     A = torch.ones(512, 64, dtype=torch.bfloat16, device=DEV)
     C = torch.empty(512, 512, dtype=torch.bfloat16, device=DEV)

@@ -37,12 +37,14 @@ def captured(fn, stream):
 
 @pytest.mark.parametrize("shape,clc", [((2304, 3072, 192), g.GEMM_CLC_OFF), ((2304, 3072, 192), g.GEMM_CLC_ON),
                                        ((16, 1024, 8192), g.GEMM_CLC_AUTO), ((300, 264, 320), g.GEMM_CLC_AUTO),
-                                       ((8, 8192, 8192), g.GEMM_CLC_AUTO)],
-                         ids=["static", "clc", "few_rows_split_k", "ragged", "two_pairs_per_cluster"])
+                                       ((8, 8192, 8192), g.GEMM_CLC_AUTO), ((2600, 3064, 4104), g.GEMM_CLC_AUTO)],
+                         ids=["static", "clc", "few_rows_split_k", "ragged", "two_pairs_per_cluster", "wide_tile"])
 def test_bf16_calls_replay_from_a_graph(shape, clc):
     M, N, K = shape
     A, B = si.bf16_problem(90, M, N, K, device=DEV)
     opts = g.options(clc=clc)
+    if shape == (2600, 3064, 4104):
+        assert g.bf16_wide_rule(M, N, K)  # the default takes the 512 x 256 tile here
     want = g.matmul_bf16(A, B, opts=opts)
     outs = [torch.zeros(M, N, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
     stream = torch.cuda.Stream(device=DEV)

@@ -43,13 +43,15 @@ def bf16_case(seed):
     opts = dict(
         clc=int(rng.choice([g.GEMM_CLC_AUTO, g.GEMM_CLC_ON, g.GEMM_CLC_OFF])),
         kernel=int(rng.choice([g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_1CTA,
-                               g.GEMM_KERNEL_BF16_2CTA_K64])),
+                               g.GEMM_KERNEL_BF16_2CTA_K64, g.GEMM_KERNEL_BF16_2CTA_WIDE])),
         max_clusters=int(rng.choice([0, 0, 0, 1, 3, 7])),
         persistent=int(rng.choice([1, 1, 1, 0])),
         no_swap_ab=int(rng.random() < 0.15),
         no_split_k=int(rng.random() < 0.15),
         no_tail_split=int(rng.random() < 0.15),
     )
+    if opts["kernel"] == g.GEMM_KERNEL_BF16_2CTA_WIDE and opts["clc"] == g.GEMM_CLC_ON:
+        opts["clc"] = g.GEMM_CLC_AUTO  # the 512 x 256 tile has a static schedule only
     return M, N, K, opts
 
 
