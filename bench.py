@@ -406,7 +406,7 @@ def default_kernel(g, cfg, props, args):
         return "2-CTA, 256 x 256 tile, 6 stages of 256 K"
     if g.bf16_plan(M, N, K)[0]:
         return "C^T = B A^T (few rows)"
-    wide = (args.epilogue == "none" and args.clc != "on" and not args.no_persistent and not args.max_clusters
+    wide = (args.clc != "on" and not args.no_persistent and not args.max_clusters
             and g.bf16_wide_rule(M, N, K, props.multi_processor_count // 2))
     return ("2-CTA, 512 x 256 tile (two 128-row M-waves per CTA), 64-K stages" if wide
             else "2-CTA, 256 x 256 tile, 128-K stages")

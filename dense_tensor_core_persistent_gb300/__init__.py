@@ -276,7 +276,7 @@ def bf16_plan(M: int, N: int, K: int, opts: gemm_options_t | None = None, epi: g
 
 def bf16_wide_rule(M: int, N: int, K: int, wave: int = 76) -> bool:
     """Whether gemm_bf16's default kernel takes the 512 x 256 pair tile for this problem
-    (plain epilogue, static schedule, not swapped), with `wave` co-resident clusters."""
+    (static schedule, not swapped), with `wave` co-resident clusters."""
     r = lib().gemm_bf16_wide_rule(M, N, K, wave)
     if r < 0:
         raise GemmError(-r, "gemm_bf16_wide_rule")

@@ -870,10 +870,10 @@ bool bf16_swap_ab(int M, int N, const RunOptions& opt) {
 }
 
 // The default kernel for a GEMM that is not swapped: the 512 x 256 pair tile where
-// wide_rule favours it, for the plain epilogue and a static schedule (the 256 x 256 kernel
-// holds the fused epilogue and cluster launch control).
+// wide_rule favours it, with a static schedule (cluster launch control, when asked for,
+// runs on the 256 x 256 kernel).
 bool bf16_use_wide(int M, int N, int K, const RunOptions& opt, int wave) {
-  if (opt.kernel != GEMM_KERNEL_DEFAULT || opt.epi.fused() || !opt.persistent || opt.max_clusters > 0) return false;
+  if (opt.kernel != GEMM_KERNEL_DEFAULT || !opt.persistent || opt.max_clusters > 0) return false;
   if (bf16_swap_ab(M, N, opt)) return false;
   if (opt.clc == 1) return false;
   return wide_rule(M, N, K, wave);

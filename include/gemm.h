@@ -208,9 +208,8 @@ typedef enum {
     GEMM_KERNEL_BF16_2CTA_K64 = 3,  /* the same with 6 stages of 64 K (4 MMAs per stage) */
     GEMM_KERNEL_BF16_2CTA_WIDE = 4  /* BF16, cta_group::2, 512 x 256 tile per CTA pair: each CTA
                                        holds 256 rows as two 128-row M-waves whose accumulators
-                                       fill TMEM; 4 stages of 64 K; static schedule and plain
-                                       epilogue only (a fused epilogue or clc = 1 is
-                                       GEMM_ERR_INVALID_ARG) */
+                                       fill TMEM; 4 stages of 64 K; static schedule only
+                                       (clc = 1 is GEMM_ERR_INVALID_ARG) */
 } gemm_kernel_t;
 
 typedef struct {
@@ -325,7 +324,7 @@ int gemm_nvfp4_blocked_fused(const void* A, const void* SFA_blocked, const void*
 int gemm_clc_rule(int items, int wave, int K, int nvfp4);
 
 /*
- * gemm_bf16_wide_rule -- whether gemm_bf16 (default kernel, plain epilogue, static schedule,
+ * gemm_bf16_wide_rule -- whether gemm_bf16 / gemm_bf16_fused (default kernel, static schedule,
  * not swapped) computes this problem on the 512 x 256 pair tile (GEMM_KERNEL_BF16_2CTA_WIDE)
  * rather than the 256 x 256 one, with `wave` co-resident clusters (76 on a 152-SM GB300).
  * Host evaluation, no GPU needed. The rule ("Achieve cuBLAS Performance on NVIDIA GB300 for

@@ -268,12 +268,9 @@ def test_default_takes_wide_tile_on_ragged_shape():
     assert_bf16_close(run(A, B), oracle.gemm_bf16(A, B), K, "default, wide tile")
 
 
-def test_wide_tile_rejects_fused_epilogue_and_clc():
+def test_wide_tile_rejects_clc():
     A = torch.ones(512, 64, dtype=torch.bfloat16, device=DEV)
     C = torch.empty(512, 512, dtype=torch.bfloat16, device=DEV)
-    with pytest.raises(g.GemmError) as e:
-        g.gemm_bf16_fused(A, A, C, 512, 512, 64, g.epilogue(alpha=2.0), opts=g.options(kernel=WIDE))
-    assert e.value.status == g.GEMM_ERR_INVALID_ARG
     with pytest.raises(g.GemmError) as e:
         g.gemm_bf16(A, A, C, 512, 512, 64, opts=g.options(kernel=WIDE, clc=g.GEMM_CLC_ON))
     assert e.value.status == g.GEMM_ERR_INVALID_ARG

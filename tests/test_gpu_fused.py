@@ -87,7 +87,7 @@ def run_bf16_fused(A, B, c_old, alpha, beta, bias, act, opts=None):
 # ---------------------------------------------------------------- BF16
 
 @pytest.mark.parametrize("variant", sorted(VARIANTS))
-@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_1CTA])
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_1CTA, g.GEMM_KERNEL_BF16_2CTA_WIDE])
 def test_bf16_fused_ragged(variant, kernel):
     M, N, K = 300, 264, 320  # ragged M and N (264 = 4 * 64 + 8), K over several stages
     A, B = si.bf16_problem(31, M, N, K)
@@ -97,17 +97,18 @@ def test_bf16_fused_ragged(variant, kernel):
     assert_fused_close(got, oracle.gemm_bf16(A, B), alpha, beta, c_old, bias, act, K, variant)
 
 
-def test_bf16_fused_integer_inputs_bit_exact():
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_2CTA_WIDE])
+def test_bf16_fused_integer_inputs_bit_exact(kernel):
     """Integer operands, power-of-two alpha and beta, integer prior C and bias: every FP32
     step is exact, so the result must equal the oracle's rounding bit for bit."""
-    M, N, K = 384, 264, 256
+    M, N, K = 600, 264, 256  # the 512 x 256 tile: the second row block holds 88 rows (one CTA, wave 0)
     A, B = si.bf16_problem(0, M, N, K, kind="int")
     c_old = torch.randint(-8, 9, (M, N), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
     c_old = c_old.view(torch.int16).numpy().view(np.uint16)
     bias = torch.randint(-16, 17, (N,), generator=torch.Generator().manual_seed(6)).to(torch.bfloat16)
     bias = bias.view(torch.int16).numpy().view(np.uint16)
     for alpha, beta, act in [(0.5, 2.0, g.GEMM_ACT_RELU), (-2.0, -0.25, g.GEMM_ACT_NONE)]:
-        got = run_bf16_fused(A, B, c_old, alpha, beta, bias, act)
+        got = run_bf16_fused(A, B, c_old, alpha, beta, bias, act, opts=g.options(kernel=kernel))
         want = oracle.round_bf16(oracle.epilogue(oracle.gemm_bf16(A, B), alpha, beta, c_old, bias, act))
         assert np.array_equal(oracle.bf16_bits_to_f64(got), oracle.bf16_bits_to_f64(want)), (alpha, beta, act)
 
@@ -124,15 +125,29 @@ def test_bf16_identity_epilogue_matches_unfused_bits():
 
 
 @pytest.mark.parametrize("max_clusters", [1, 3])
-def test_bf16_fused_many_tiles_per_cluster(max_clusters):
+@pytest.mark.parametrize("kernel", [g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_2CTA_WIDE])
+def test_bf16_fused_many_tiles_per_cluster(max_clusters, kernel):
     """Each epilogue warp loads the prior C of many chunks and tiles: its load barrier's
     phase alternates across tiles."""
     M, N, K = 1280, 1024, 256
     A, B = si.bf16_problem(35, M, N, K)
     c_old = prior_c(M, N, 36)
     bias = bias_bits(N, 37)
-    got = run_bf16_fused(A, B, c_old, 1.5, -1.0, bias, g.GEMM_ACT_GELU_TANH, opts=g.options(max_clusters=max_clusters))
+    got = run_bf16_fused(A, B, c_old, 1.5, -1.0, bias, g.GEMM_ACT_GELU_TANH,
+                         opts=g.options(max_clusters=max_clusters, kernel=kernel))
     assert_fused_close(got, oracle.gemm_bf16(A, B), 1.5, -1.0, c_old, bias, g.GEMM_ACT_GELU_TANH, K, "many tiles")
+
+
+def test_bf16_fused_default_wide_tile():
+    """A fused call at a shape where the default takes the 512 x 256 tile (ragged in M, N
+    and K), with alpha, beta, bias and GELU."""
+    M, N, K = 2600, 3064, 4104
+    assert g.bf16_wide_rule(M, N, K)
+    A, B = si.bf16_problem(38, M, N, K)
+    c_old = prior_c(M, N, 39)
+    bias = bias_bits(N, 40)
+    got = run_bf16_fused(A, B, c_old, -1.25, 1.5, bias, g.GEMM_ACT_GELU_TANH)
+    assert_fused_close(got, oracle.gemm_bf16(A, B), -1.25, 1.5, c_old, bias, g.GEMM_ACT_GELU_TANH, K, "default wide")
 
 
 # ---------------------------------------------------------------- NVFP4
