@@ -88,10 +88,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, uuid: str | None):
+    def __init__(self, uuid: str | None, start: bool = True):
         self.rows = []
         self.proc = None
         self.t0 = self.t1 = None
+        if not start:  # rows supplied by the caller (tests)
+            return
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
         if uuid:
             cmd += ["-i", uuid]
@@ -159,7 +161,7 @@ class ClockSampler:
         shorter than the sampling period and none falls inside, sm_mhz is null and says so
         (`after`, if given, is the window of a continuation of the same launches after the
         timed region, reported separately and labelled as such)."""
-        if self.proc is None:
+        if self.proc is None and not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.stop()
         out = self.window(self.t0, self.t1)
