@@ -1,4 +1,6 @@
-// gemm_bf16.cu -- BF16 C = A * B^T on sm_103a tensor cores (tcgen05), FP32 accumulation.
+// gemm_bf16.cu -- BF16 C = A * B^T on sm_103a tensor cores (tcgen05), FP32 accumulation:
+// the 256 x 256 pair tile (and its 1-CTA, swapped few-row and split-K variants) and the
+// host dispatch between it and the 512 x 256 pair tile of gemm_bf16_wide.cu.
 //
 // One persistent, warp-specialised kernel template:
 //   warp 0      TMA producer of A: fills an S-stage shared-memory ring with A K-slices and

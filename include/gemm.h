@@ -72,9 +72,10 @@ typedef enum {
  * M and N need not be tile multiples: rows/columns past M/N are read as zeros
  * and never written. M == 0 or N == 0: nothing to do, returns GEMM_OK.
  * K == 0: C is set to zero (an empty sum).
- * Kernel: persistent, warp-specialised, 2-CTA (cta_group::2) tcgen05 MMA with
- * a 256 x 256 output tile per CTA pair, double-buffered TMEM accumulator and a
- * TMA-store epilogue; one kernel launch per call. With M <= 128 and N >= 256 it
+ * Kernel: persistent, warp-specialised, 2-CTA (cta_group::2) tcgen05 MMA with a
+ * TMA-store epilogue, one kernel launch per call: a 512 x 256 output tile per CTA pair
+ * (two 128-row M-waves per CTA filling TMEM) where gemm_bf16_wide_rule selects it, else
+ * a 256 x 256 tile with a double-buffered TMEM accumulator. With M <= 128 and N >= 256 it
  * computes C^T = B A^T instead (tile N 64 or 128; see gemm_options_t.no_swap_ab), and
  * such a GEMM with few tiles splits K: the FP32 partial sums are added by a second launch
  * or, for two splits, inside the one launch (workspace from the library's stream-ordered
@@ -204,7 +205,8 @@ typedef enum {
     GEMM_KERNEL_DEFAULT = 0,        /* what gemm_bf16 / gemm_nvfp4 launch */
     GEMM_KERNEL_BF16_1CTA = 1,      /* BF16, cta_group::1, 128 x 256 tile per CTA */
     GEMM_KERNEL_BF16_2CTA = 2,      /* BF16, cta_group::2, 256 x 256 tile per CTA pair, 3 stages of
-                                       128 K (8 MMAs per stage): the default */
+                                       128 K (8 MMAs per stage), double-buffered accumulator: the
+                                       default where gemm_bf16_wide_rule does not select the wide tile */
     GEMM_KERNEL_BF16_2CTA_K64 = 3,  /* the same with 6 stages of 64 K (4 MMAs per stage) */
     GEMM_KERNEL_BF16_2CTA_WIDE = 4  /* BF16, cta_group::2, 512 x 256 tile per CTA pair: each CTA
                                        holds 256 rows as two 128-row M-waves whose accumulators
