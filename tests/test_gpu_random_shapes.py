@@ -4,8 +4,9 @@ Each case draws M, N, K (ragged, within the layout rules: N % 8 == 0, BF16 K % 8
 NVFP4 K % 256 == 0) and a set of options: the scheduler (static, CLC), the kernel
 variant, a cluster cap, one tile per cluster, swap-AB and split-K switches and the tail
 split. Together they reach the swapped few-row path with and without K splits (through
-the reduction kernel or a cluster of two CTA pairs), split tails, CLC cancellations and
-ragged edges in every dimension. Sizes stay small enough for the oracle to take about a
+the reduction kernel or a cluster of two CTA pairs), split tails, CLC cancellations, the
+512 x 256 BF16 tile (plain and fused), few-row NVFP4 GEMMs with and without the padded copy
+of A, and ragged edges in every dimension. Sizes stay small enough for the oracle to take about a
 second per case.
 """
 import numpy as np
@@ -69,11 +70,12 @@ def test_bf16_random_shape_and_options(seed):
 @pytest.mark.parametrize("seed", range(32))
 def test_nvfp4_random_shape_and_options(seed):
     rng = np.random.default_rng(2000 + seed)
-    M = int(rng.integers(1, 600))
+    M = int(rng.integers(1, 32)) if seed % 4 == 3 else int(rng.integers(1, 600))  # a quarter with few rows
     N = 8 * int(rng.integers(1, 120))
     K = 256 * int(rng.integers(1, 9))
     opts = dict(clc=int(rng.choice([g.GEMM_CLC_AUTO, g.GEMM_CLC_ON])), max_clusters=int(rng.choice([0, 0, 2, 5])),
-                persistent=int(rng.choice([1, 1, 0])), no_tail_split=int(rng.random() < 0.2))
+                persistent=int(rng.choice([1, 1, 0])), no_tail_split=int(rng.random() < 0.2),
+                no_pad_a=int(rng.random() < 0.3))
     a, sfa, b, sfb = si.nvfp4_problem(seed, M, N, K)
     C = g.matmul_nvfp4(a.to(DEV), sfa.to(DEV), b.to(DEV), sfb.to(DEV), opts=g.options(**opts))
     torch.cuda.synchronize()
@@ -92,7 +94,9 @@ def test_bf16_fused_random_shape_and_epilogue(seed):
     act = int(rng.choice([g.GEMM_ACT_NONE, g.GEMM_ACT_RELU, g.GEMM_ACT_GELU_TANH]))
     bias = bias_bits(N, 3100 + seed) if rng.random() < 0.5 else None
     c_old = prior_c(M, N, 3200 + seed)
-    opts = g.options(clc=int(rng.choice([g.GEMM_CLC_AUTO, g.GEMM_CLC_ON])), max_clusters=int(rng.choice([0, 3])))
+    kernel = int(rng.choice([g.GEMM_KERNEL_DEFAULT, g.GEMM_KERNEL_BF16_2CTA_WIDE]))
+    clc = int(rng.choice([g.GEMM_CLC_AUTO, g.GEMM_CLC_ON])) if kernel == g.GEMM_KERNEL_DEFAULT else g.GEMM_CLC_AUTO
+    opts = g.options(clc=clc, max_clusters=int(rng.choice([0, 3])), kernel=kernel)
     A, B = si.bf16_problem(3300 + seed, M, N, K)
     got = run_bf16_fused(A, B, c_old, alpha, beta, bias, act, opts=opts)
     assert_fused_close(got, oracle.gemm_bf16(A, B), alpha, beta, c_old, bias, act, K, f"{M}x{N}x{K}")
