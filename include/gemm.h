@@ -247,13 +247,12 @@ typedef struct {
                             co-resident clusters walk the items with a fixed stride */
     int no_pad_a;        /* NVFP4 with 1 <= M < 32 (gemm_nvfp4*, gemm_nvfp4_blocked*): 0 = A's M rows
                             are first copied (by the scale-packing launch, or by a small copy
-                            kernel) into a 32-row buffer from the library's stream-ordered pool
-                            (measured on GB300: 46.1 -> 34.9 us at M = 1, N = 28672, K = 8192,
-                            blocked scales), and the GEMM
-                            reads A from there (rows M..31 are not written; they only reach C
-                            rows that are never stored): spread over 32 rows, A's lines no
-                            longer all fall in the few L2 slices that every CTA pair reads at
-                            once; 1 = never (A read in place, no allocation) */
+                            kernel) into a 32-row buffer from the library's stream-ordered pool,
+                            and the GEMM reads A from there (rows M..31 are not written; they
+                            only reach C rows that are never stored). All CTA pairs reading an
+                            A that spans fewer than 32 rows of codes ran measurably slower on
+                            GB300 (46.1 -> 31.9 us at M = 1, N = 28672, K = 8192, blocked
+                            scales); 1 = never (A read in place, no allocation) */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */
