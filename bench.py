@@ -276,6 +276,23 @@ def launch(g, cfg, ins, C, stream, opts, scales="rowmajor", epi=None):
         g.gemm_nvfp4(ins[0], ins[1], ins[2], ins[3], C, M, N, K, stream, opts)
 
 
+PROBE_CTAS = 4096  # clock-probe records per launch (the persistent grids use at most 152 CTAs)
+
+
+def summarize_probes(g, probes):
+    """Median over the probed launches of each launch's median CTA clock (MHz)."""
+    per = [g.clock_probe_mhz(p) for p in probes]
+    per = [r for r in per if r.get("ctas")]
+    if not per:
+        return None
+    mhz = sorted(r["sm_mhz"] for r in per)
+    return {"sm_mhz": mhz[len(mhz) // 2], "sm_mhz_min": mhz[0], "sm_mhz_max": mhz[-1], "launches_probed": len(per),
+            "ctas_per_launch": per[0]["ctas"],
+            "what": ("SM clock inside the GEMM: each CTA's clock64 over %globaltimer from the start to the end of "
+                     "its work (median over the CTAs), on every launch of the timed region that carried a probe "
+                     "(gemm_options_t.clock_probe; median over those launches)")}
+
+
 def cpu_model() -> str:
     """The host CPU's model, from /proc/cpuinfo (x86: "model name"; Arm: implementer and part codes)."""
     try:
@@ -475,6 +492,21 @@ def run_ours(args, cfg, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     launches0 = g.launch_count()
+    # The SM clock inside the GEMM, from its own CTAs: every `stride`-th launch of the timed
+    # region (at most 64 of them) carries a clock probe (gemm_options_t.clock_probe: each
+    # CTA stores clock64 and %globaltimer at the start and end of its work, 4 stores per
+    # CTA). nvidia-smi samples about every 100 ms and sees nothing of a burst of launches.
+    probes, probe_opts = [], {}
+    if graph is None:
+        stride = max(1, -(-args.steps // 64))
+        for i in range(0, args.steps, stride):
+            buf = torch.zeros(4 * PROBE_CTAS, dtype=torch.int64, device=dev)
+            probes.append(buf)
+            probe_opts[i] = g.options(kernel=args.kernel, group_m=args.group_m, max_clusters=args.max_clusters,
+                                      persistent=0 if args.no_persistent else 1,
+                                      no_tail_split=1 if args.no_tail_split else 0, no_pdl=1 if args.no_pdl else 0,
+                                      clc=CLC_MODES[args.clc], clock_probe=buf)
+        torch.cuda.synchronize()
     if clocks:
         clocks.mark_start()
     ev0.record(stream)
@@ -483,7 +515,7 @@ def run_ours(args, cfg, world, rank, local):
             graph.replay()
     else:
         for i in range(args.steps):
-            launch(g, cfg, sets[i % R], outs[i % R], stream, opts, args.scales, epi)
+            launch(g, cfg, sets[i % R], outs[i % R], stream, probe_opts.get(i, opts), args.scales, epi)
     ev1.record(stream)
     stream.synchronize()
     if clocks:
@@ -496,6 +528,7 @@ def run_ours(args, cfg, world, rank, local):
     st, detail = g.get_device_status(stream)
     if st != 0:
         raise RuntimeError(f"kernel status {st} ({detail:#x}) in the timed region")
+    kernel_clock = summarize_probes(g, probes) if probes else None
     after = None
     if clocks and (clocks.t1 - clocks.t0) < ClockSampler.MIN_REGION_S:
         # A timed region too short for the sampler: the same launches continue, untimed, for
@@ -592,6 +625,11 @@ def run_ours(args, cfg, world, rank, local):
             ceiling = fpc * props.multi_processor_count * mhz * 1e6 / 1e12
             rate.update({"ceiling_at_sampled_clock": ceiling, "frac_of_ceiling": achieved / ceiling,
                          "clock_mhz": mhz, "clock_from": clock_src})
+        if kernel_clock and kernel_clock.get("sm_mhz"):
+            kc = kernel_clock["sm_mhz"]
+            ceiling = fpc * props.multi_processor_count * kc * 1e6 / 1e12
+            rate.update({"ceiling_at_kernel_clock": ceiling, "frac_of_ceiling_at_kernel_clock": achieved / ceiling,
+                         "kernel_clock_mhz": kc})
     except Exception as e:  # report, do not fail the benchmark line
         rate = {"error": str(e)}
     # the recorded counters are those of the plain kernel
@@ -660,7 +698,7 @@ def run_ours(args, cfg, world, rank, local):
                 "pipelining": "copy-in of step i+1 and copy-out of step i-1 overlap the GEMM of step i "
                               "(3 streams, 2 device buffer sets, pinned host memory)"},
         "gpu_launches": int(launches),
-        "clocks": clock_info,
+        "clocks": dict(clock_info or {}, kernel=kernel_clock) if kernel_clock else clock_info,
     }
     print(json.dumps(line), flush=True)
 

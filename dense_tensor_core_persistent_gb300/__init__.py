@@ -71,6 +71,8 @@ class gemm_options_t(ctypes.Structure):
         ("no_split_k", ctypes.c_int),
         ("clc", ctypes.c_int),
         ("no_pad_a", ctypes.c_int),
+        ("clock_probe", ctypes.c_void_p),
+        ("clock_probe_ctas", ctypes.c_int),
     ]
 
 
@@ -81,9 +83,27 @@ GEMM_CLC_OFF = 2
 
 
 def options(kernel=GEMM_KERNEL_DEFAULT, persistent=1, group_m=0, max_clusters=0, wait_limit_us=0, debug_flags=0,
-            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0, clc=GEMM_CLC_AUTO, no_pad_a=0):
+            no_tail_split=0, no_pdl=0, no_swap_ab=0, no_split_k=0, clc=GEMM_CLC_AUTO, no_pad_a=0, clock_probe=None):
+    """`clock_probe`: None, or a CUDA int64 tensor of 4 values per CTA (see clock_probe_mhz)."""
+    probe, probe_ctas = None, 0
+    if clock_probe is not None:
+        probe, probe_ctas = _ptr(clock_probe), clock_probe.numel() // 4
     return gemm_options_t(kernel, persistent, group_m, max_clusters, wait_limit_us, debug_flags, no_tail_split, no_pdl,
-                          no_swap_ab, no_split_k, clc, no_pad_a)
+                          no_swap_ab, no_split_k, clc, no_pad_a, probe, probe_ctas)
+
+
+def clock_probe_mhz(probe) -> dict:
+    """Reads a clock probe after the launch completed (gemm_options_t.clock_probe): each CTA's
+    SM clock over its work (clock64 difference / %globaltimer difference), the median and
+    range over the CTAs that recorded, and the span from the first start to the last end."""
+    v = probe.view(-1, 4).cpu().tolist()
+    rec = [r for r in v if r[0] and r[2] > r[0]]
+    if not rec:
+        return {"ctas": 0}
+    mhz = sorted((r[3] - r[1]) / (r[2] - r[0]) * 1e3 for r in rec)
+    span_us = (max(r[2] for r in rec) - min(r[0] for r in rec)) / 1e3
+    return {"ctas": len(rec), "sm_mhz": mhz[len(mhz) // 2], "sm_mhz_min": mhz[0], "sm_mhz_max": mhz[-1],
+            "span_us": span_us}
 
 
 class gemm_epilogue_t(ctypes.Structure):

@@ -228,6 +228,7 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   if (o->no_tail_split != 0 && o->no_tail_split != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pdl != 0 && o->no_pdl != 1) return GEMM_ERR_INVALID_ARG;
   if (o->no_pad_a != 0 && o->no_pad_a != 1) return GEMM_ERR_INVALID_ARG;
+  if (o->clock_probe_ctas < 0 || (o->clock_probe_ctas > 0 && o->clock_probe == nullptr)) return GEMM_ERR_INVALID_ARG;
   if (o->kernel < GEMM_KERNEL_DEFAULT || o->kernel > GEMM_KERNEL_BF16_2CTA_WIDE) return GEMM_ERR_INVALID_ARG;
   if (o->group_m < 0 || o->max_clusters < 0 || (o->persistent != 0 && o->persistent != 1))
     return GEMM_ERR_INVALID_ARG;
@@ -242,6 +243,8 @@ static int resolve_options(const gemm_options_t* o, RunOptions* r) {
   r->split_k = o->no_split_k ? 0 : 1;
   r->clc = o->clc;
   r->pad_a = o->no_pad_a ? 0 : 1;
+  r->clock_probe = o->clock_probe_ctas > 0 ? o->clock_probe : nullptr;
+  r->clock_probe_ctas = o->clock_probe_ctas;
   if (o->wait_limit_us != 0) r->wait_limit_ns = uint64_t(o->wait_limit_us) * 1000ull;
   r->debug_flags = o->debug_flags;
   return GEMM_OK;

@@ -186,6 +186,23 @@ __device__ __forceinline__ int clc_next(const ClcRing& r, int t, int cg, bool ar
   return got ? static_cast<int>(x) / cg : -1;
 }
 
+// ---------------------------------------------------------------- clock probe
+
+// gemm_options_t.clock_probe: thread 0 of each CTA (blockIdx.x < ctas) stores %globaltimer
+// and the SM's clock64 when its work starts (after the dependency wait, slot 0) and when
+// it ends (after the teardown barrier, slot 1): buf[4 b + 2 slot] and buf[4 b + 2 slot + 1].
+// The ratio of the differences is the SM clock the CTA ran at. Null buf: nothing is stored.
+struct ClockProbe {
+  unsigned long long* buf;
+  int ctas;
+};
+__device__ __forceinline__ void clock_probe_mark(const ClockProbe& c, int slot) {
+  if (c.buf != nullptr && threadIdx.x == 0 && static_cast<int>(blockIdx.x) < c.ctas) {
+    c.buf[4 * blockIdx.x + 2 * slot] = globaltimer_ns();
+    c.buf[4 * blockIdx.x + 2 * slot + 1] = static_cast<unsigned long long>(clock64());
+  }
+}
+
 // ---------------------------------------------------------------- fused epilogue
 
 // C = act(alpha * acc + beta * C_old + bias[col]), in FP32, rounded once to BF16.

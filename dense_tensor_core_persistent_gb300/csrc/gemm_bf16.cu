@@ -65,6 +65,7 @@ struct Bf16Params {
   int splits, k_per_split, ldw;
   float* ws;
   int clc;  // 1: one cluster per item is launched; running clusters take the items of clusters they cancel
+  ClockProbe probe;
 };
 
 struct Bf16Item {
@@ -222,6 +223,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
   // loads and stores) comes after the previous kernel on the stream has completed.
   pdl_launch_dependents();
   pdl_wait();
+  clock_probe_mark(p.probe, 0);
 
   if (warp == 0 || warp == L::WARP_PROD_B) {
     // ------------------------------------------------------------ TMA producers (A: warp 0, B)
@@ -612,6 +614,7 @@ __global__ void __launch_bounds__(Bf16Layout<CG, STAGES, ATOMS, BN, SWAP>::NUM_T
     tc_fence_after_sync();
     tmem_dealloc<CG>(tmem_base, L::TMEM_COLS);
   }
+  clock_probe_mark(p.probe, 1);
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -765,6 +768,7 @@ struct Bf16Variant {
     p.epi.bias = static_cast<const uint16_t*>(opt.epi.bias);
     p.epi.act = opt.epi.act;
     p.epi.fused = opt.epi.fused() ? 1 : 0;
+    p.probe = ClockProbe{opt.clock_probe, opt.clock_probe_ctas};
     if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
     const int max_clusters = max_active_clusters(device);

@@ -51,6 +51,7 @@ struct WideParams {
   unsigned debug_flags;
   int zigzag;
   EpiParams epi;  // fused epilogue (the FUSED instantiation)
+  ClockProbe probe;
 };
 
 struct WideLayout {
@@ -461,6 +462,7 @@ __global__ void __launch_bounds__(WideLayout::NUM_THREADS, 1)
   // loads and stores) comes after the previous kernel on the stream has completed.
   pdl_launch_dependents();
   pdl_wait();
+  clock_probe_mark(p.probe, 0);
 
   // One branch per role group, each running to the end of the kernel (with FUSED, the
   // code after a change of register limit belongs to that limit).
@@ -475,6 +477,7 @@ __global__ void __launch_bounds__(WideLayout::NUM_THREADS, 1)
     }
     __syncwarp();
     wide_teardown(warp, tmem_base);
+    clock_probe_mark(p.probe, 1);
   } else {
     if constexpr (FUSED) regs_increase<L::REGS_EPI>();
     wide_epilogue<FUSED>(p, &tmap_c, base, tmem_base, warp, lane, rank, cluster_idx, num_clusters, wctx);
@@ -557,6 +560,7 @@ int run_gemm_bf16_wide(const void* A, const void* B, void* C, int M, int N, int 
   p.epi.bias = static_cast<const uint16_t*>(opt.epi.bias);
   p.epi.act = opt.epi.act;
   p.epi.fused = opt.epi.fused() ? 1 : 0;
+  p.probe = ClockProbe{opt.clock_probe, opt.clock_probe_ctas};
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = wide_max_active_clusters(device);

@@ -66,6 +66,7 @@ struct Nvfp4Params {
   int wave;       // co-resident clusters
   int clc;        // 1: one cluster per item is launched; running clusters take the items of clusters they cancel
   EpiParams epi;  // fused epilogue (epi.fused == 0: plain BF16 rounding)
+  ClockProbe probe;
 };
 
 template <int STAGES>
@@ -627,6 +628,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
   // loads and stores) comes after the previous kernel on the stream has completed.
   pdl_launch_dependents();
   pdl_wait();
+  clock_probe_mark(p.probe, 0);
 
   // One branch per warpgroup, each with one register-limit change for all its warps: the
   // epilogue warpgroup takes the registers that warpgroups 0 and 2 give up. Each branch
@@ -637,6 +639,7 @@ __global__ void __launch_bounds__(Nvfp4Layout<STAGES>::NUM_THREADS, 1)
     else mma_role<STAGES>(p, x);
     __syncwarp();
     teardown<STAGES>(x);
+    clock_probe_mark(p.probe, 1);
   } else if (x.warp < L::COPY_WARP0) {
     regs_increase<L::REGS_EPI>();
     epilogue_role<STAGES, FUSED>(p, &tmap_c, x);
@@ -745,6 +748,7 @@ int run_gemm_nvfp4_blocked(const void* A, const void* SFA, const void* B, const 
   p.epi.bias = static_cast<const uint16_t*>(opt.epi.bias);
   p.epi.act = opt.epi.act;
   p.epi.fused = opt.epi.fused() ? 1 : 0;
+  p.probe = ClockProbe{opt.clock_probe, opt.clock_probe_ctas};
   if (p.status == nullptr) return GEMM_ERR_NO_DEVICE;
 
   const int max_clusters = max_active_clusters(device);

@@ -57,6 +57,8 @@ struct RunOptions {
   int split_k = 1;  // allow K splits for the swapped BF16 GEMMs
   int clc = 0;      // cluster launch control: 0 = by clc_rule, 1 = on, 2 = off
   int pad_a = 1;    // NVFP4 with 1 <= M < kNvfp4PadRows: read A from a padded copy
+  unsigned long long* clock_probe = nullptr;  // gemm_options_t.clock_probe (GEMM kernels only)
+  int clock_probe_ctas = 0;
   uint64_t wait_limit_ns = 2000000000ull;
   uint32_t debug_flags = 0;
   EpilogueOptions epi;

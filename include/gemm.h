@@ -253,6 +253,18 @@ typedef struct {
                             A that spans fewer than 32 rows of codes ran measurably slower on
                             GB300 (46.1 -> 31.9 us at M = 1, N = 28672, K = 8192, blocked
                             scales); 1 = never (A read in place, no allocation) */
+    unsigned long long* clock_probe; /* NULL in production. Else device memory of 4 values per CTA
+                            for the GEMM kernel's launch (not the scale-packing, copy or
+                            split-K reduction kernels): thread 0 of CTA b (b < clock_probe_ctas)
+                            stores at [4b] %globaltimer (ns) and at [4b+1] the SM's clock64
+                            when its work starts (after waiting for the previous kernel on
+                            the stream), and at [4b+2], [4b+3] the same when it ends (after
+                            its teardown barrier). (dclock / dtime) is the SM clock the CTA
+                            ran at: nvidia-smi samples every 100 ms or so and cannot see a
+                            burst of a few launches. The caller owns the buffer; a call that
+                            launches several GEMMs (a K split) overwrites it */
+    int clock_probe_ctas; /* CTAs the buffer holds (>= 0; CTAs beyond it store nothing); must be 0
+                            when clock_probe is NULL */
 } gemm_options_t;
 
 /* gemm_bf16 with explicit options (NULL options = defaults). Same contract as gemm_bf16. */

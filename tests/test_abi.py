@@ -192,6 +192,21 @@ def test_nvfp4_plan_pads_a_for_few_rows():
     assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
 
 
+def test_clock_probe_options_checked():
+    """gemm_options_t.clock_probe: a negative CTA count, or a count without a buffer, is
+    GEMM_ERR_INVALID_ARG (checked on the host before any launch)."""
+    import ctypes
+    out = ctypes.c_int()
+    o = g.options()
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_OK
+    o.clock_probe_ctas = -1
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    o.clock_probe_ctas = 4  # no buffer
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_ERR_INVALID_ARG
+    o.clock_probe = 256  # any non-null address passes the host check (the kernel writes it)
+    assert g.lib().gemm_nvfp4_plan(1, 8, 256, ctypes.byref(o), ctypes.byref(out)) == g.GEMM_OK
+
+
 def test_bf16_wide_rule():
     """The 512 x 256 pair tile where its fewer, larger tiles still fill the 76 clusters."""
     assert g.bf16_wide_rule(8192, 8192, 8192)          # 512 wide tiles: 7 waves vs 13.8
