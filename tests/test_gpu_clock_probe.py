@@ -51,10 +51,11 @@ def timed(fn):
     return e0.elapsed_time(e1)
 
 
+# K = 8192: every CTA works for tens of microseconds, long against the timer's granularity
 @pytest.mark.parametrize("kernel,shape", [
-    (g.GEMM_KERNEL_BF16_2CTA_WIDE, (2048, 2048, 1024)),  # 16 tiles of 512 x 256 (as N-halves)
-    (g.GEMM_KERNEL_BF16_2CTA, (1024, 1024, 512)),        # 16 tiles of 256 x 256 (as N-halves)
-    (g.GEMM_KERNEL_BF16_1CTA, (512, 512, 256)),          # 8 tiles of 128 x 256, one CTA each
+    (g.GEMM_KERNEL_BF16_2CTA_WIDE, (2048, 2048, 8192)),  # 16 tiles of 512 x 256 (as N-halves)
+    (g.GEMM_KERNEL_BF16_2CTA, (1024, 1024, 8192)),       # 16 tiles of 256 x 256 (as N-halves)
+    (g.GEMM_KERNEL_BF16_1CTA, (512, 512, 8192)),         # 8 tiles of 128 x 256, one CTA each
 ], ids=["wide", "pair", "single_cta"])
 def test_bf16_kernels_record_every_cta(kernel, shape):
     M, N, K = shape
@@ -70,7 +71,7 @@ def test_bf16_kernels_record_every_cta(kernel, shape):
 
 
 def test_nvfp4_kernel_records_every_cta():
-    M, N, K = 512, 1024, 512  # 8 tiles of 256 x 256 (the scale-packing kernel records nothing)
+    M, N, K = 512, 1024, 8192  # 8 tiles of 256 x 256 (the scale-packing kernel records nothing)
     a, sfa, b, sfb = si.nvfp4_problem(71, M, N, K)
     probe = torch.zeros(4 * 4096, dtype=torch.int64, device=DEV)
     ins = [t.to(DEV) for t in (a, sfa, b, sfb)]
