@@ -258,6 +258,16 @@ def test_few_rows_read_a_from_padded_copy(shape, path):
     assert np.array_equal(padded, run(a, sfa, b, sfb, path, no_pad_a=1))
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("shape", [(1, 28672, 8192), (16, 28672, 8192)], ids=lambda s: "x".join(map(str, s)))
+def test_few_rows_full_size_every_element(shape, path):
+    """A decode-sized NVFP4 GEMM (one or 16 rows against a 28672 x 8192 weight): every output
+    against the oracle, through the padded copy of A (the default)."""
+    M, N, K = shape
+    a, sfa, b, sfb = si.nvfp4_problem(M + 7, M, N, K)
+    assert_nvfp4_close(run(a, sfa, b, sfb, path), oracle.gemm_nvfp4(a, sfa, b, sfb), f"{shape} {path}")
+
+
 def test_few_rows_launches_per_call():
     """Fewer than 32 rows: gemm_nvfp4's packing launch also copies A (2 launches in all);
     gemm_nvfp4_blocked launches a copy kernel before the GEMM (2); with no_pad_a, 2 and 1."""
