@@ -35,7 +35,7 @@ CONFIGS = {
 }
 # The page's own number for this metric and workload: "Achieve cuBLAS Performance on NVIDIA
 # GB300 for HGEMM", Performance table, v7 at M = N = K = 8192 on GB300.
-PAGE_BASELINE = {"c3": 1980.925}
+PAGE_TFLOPS = {"c3": 1980.925}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 CLC_MODES = {"auto": 0, "on": 1, "off": 2}   # gemm_options_t.clc
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25   # nominal dense FP4 / BF16 tensor rates (6x)
@@ -639,7 +639,7 @@ def run_ours(args, cfg, world, rank, local):
     if cpu:
         cpu.pop("seconds", None)
         cpu.pop("rows", None)
-    baseline = PAGE_BASELINE.get(args.config)
+    baseline = PAGE_TFLOPS.get(args.config)
     line = {
         "metric": metric_name(cfg),
         "value": value,
